@@ -1,0 +1,482 @@
+// Host side of the C ABI declared in include/smq.h: argument validation, the
+// plan, TMA tensor-map encoding and kernel launches. Nothing here allocates
+// device memory; every tensor is the caller's.
+#include "smq.h"
+#include "smq_kernels.cuh"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+using smq::kHeadDim;
+using smq::kTileM;
+
+struct smq_plan {
+  smq_plan_desc desc;
+  int32_t sbkv;
+  int32_t nsb;
+  int32_t num_cols;
+  int32_t page_bytes;
+  int32_t num_sms;
+  int32_t n_mma;
+  bool prepared;
+};
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int pick_sbkv(int page_size, int cbs) {
+  for (int s : {128, 64, 32, 16})
+    if (page_size % s == 0 && cbs % s == 0) return s;
+  return 0;
+}
+
+// Q viewed as [rows * H][128] bytes; one box = one row's H heads, padded to the MMA N.
+int encode_q(CUtensorMap* m, const uint8_t* q, int64_t qrows, int n_mma) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SMQ_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(qrows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(n_mma)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+// Paged cache values: [num_pages][page_size][128 FP4] with page stride page_bytes,
+// unpacked on load to 16-byte containers (8 data bytes + 8 pad) for the MMA.
+int encode_k_paged(CUtensorMap* m, const uint8_t* cache, int page_size, int64_t num_pages, int64_t page_bytes,
+                   int sbkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SMQ_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(page_size),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim / 2), static_cast<cuuint64_t>(page_bytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(sbkv), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+// Contiguous workspace values [total_len][128 FP4], same unpacking.
+int encode_k_contig(CUtensorMap* m, const uint8_t* values, int64_t total_len, int sbkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SMQ_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(total_len)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim / 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(sbkv)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(values), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+// Contiguous workspace scales as one 32-bit word per position. A box of
+// sbkv + 4 words starts at a multiple of 4 positions so that every load
+// starts on a 16-byte boundary; the kernel indexes past the remainder.
+int encode_k_scales(CUtensorMap* m, const uint8_t* scales, int64_t total_len, int sbkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SMQ_ERR_CUDA;
+  cuuint64_t dims[1] = {static_cast<cuuint64_t>(total_len)};
+  cuuint64_t strides[1] = {0};
+  cuuint32_t box[1] = {static_cast<cuuint32_t>(sbkv + 4)};
+  cuuint32_t es[1] = {1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 1, const_cast<uint8_t*>(scales), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+constexpr size_t kStatusBytes = 256;
+
+size_t workspace_bytes_for(const smq_plan* p, int64_t rows) {
+  return kStatusBytes + static_cast<size_t>(rows) * p->num_cols * sizeof(float);
+}
+
+int check_device(smq_plan* p) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (dev != p->desc.device) return SMQ_ERR_INVALID_ARG;
+  if (!p->prepared) {
+    if (smq::prepare_kernels(p->n_mma) != cudaSuccess) return SMQ_ERR_CUDA;
+    p->prepared = true;
+  }
+  return SMQ_OK;
+}
+
+// Pipeline depth that fits the opt-in shared memory for this many rows.
+int pick_stages(const smq_plan* p, int rows) {
+  const size_t limit = 232448;
+  for (int st = 8; st >= 2; --st)
+    if (smq::score_smem_bytes(p->n_mma, p->desc.num_heads, p->sbkv, st, rows) <= limit) return st;
+  return 0;
+}
+
+int tmem_cols_for(int n_mma, int stages) {
+  const int need = 2 * n_mma + 4 * stages + 4;
+  int c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
+// Record a caller's profiling event. Inside a stream capture it becomes an
+// external event-record node, so that graph replays stamp it.
+void record(void* ev, cudaStream_t s) {
+  if (!ev) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+struct CommonRows {
+  int32_t rows;
+  const uint8_t* q;
+  const float* q_scale;
+  const uint16_t* weights;
+  const int32_t* candidate_blocks;
+  int32_t* topk_out;
+  int32_t topk_ld;
+  int32_t* sparse_indices;
+  int32_t* end;
+  int32_t expansion_ready;
+  int32_t* col_indices;
+  float* logits_out;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+int check_common(const smq_plan* p, const CommonRows& a) {
+  if (a.rows < 0 || a.rows > p->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  if (a.rows == 0) return SMQ_OK;
+  if (!a.q || !a.q_scale || !a.weights || !a.topk_out || !a.sparse_indices || !a.end || !a.workspace)
+    return SMQ_ERR_INVALID_ARG;
+  if (!a.expansion_ready && !a.candidate_blocks) return SMQ_ERR_INVALID_ARG;
+  if (a.topk_ld < p->desc.topk) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.weights, 16) || !aligned(a.workspace, 16) || !aligned(a.q_scale, 4) ||
+      !aligned(a.topk_out, 4) || !aligned(a.sparse_indices, 4) || !aligned(a.end, 4))
+    return SMQ_ERR_INVALID_ARG;
+  if (a.logits_out && !aligned(a.logits_out, 4)) return SMQ_ERR_INVALID_ARG;
+  if (a.workspace_bytes < workspace_bytes_for(p, a.rows)) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  return SMQ_OK;
+}
+
+smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a, int stages) {
+  smq::ScoreParams s;
+  std::memset(&s, 0, sizeof s);
+  s.rows = a.rows;
+  s.heads = p->desc.num_heads;
+  s.n_mma = p->n_mma;
+  s.sbkv = p->sbkv;
+  s.subs_per_tile = kTileM / p->sbkv;
+  s.nsb = p->nsb;
+  s.num_cols = p->num_cols;
+  s.stages = stages;
+  s.tmem_cols = tmem_cols_for(p->n_mma, stages);
+  s.q_scale = a.q_scale;
+  s.weights = a.weights;
+  s.sparse_indices = a.sparse_indices;
+  s.end = a.end;
+  s.status = static_cast<int32_t*>(a.workspace);
+  s.logits = a.logits_out ? a.logits_out
+                          : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes);
+  return s;
+}
+
+int run_expand(const smq_plan* p, const int32_t* cand, const int32_t* ks, const int32_t* ke, int rows, int32_t* si,
+               int32_t* end, cudaStream_t stream) {
+  smq::ExpandParams e;
+  e.rows = rows;
+  e.ncb = p->desc.candidate_topk_blocks;
+  e.cbs = p->desc.candidate_block_size;
+  e.sbkv = p->sbkv;
+  e.nsb = p->nsb;
+  e.candidate_blocks = cand;
+  e.row_ks = ks;
+  e.row_ke = ke;
+  e.sparse_indices = si;
+  e.end = end;
+  return smq::launch_expand(e, stream) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+int run_topk(const smq_plan* p, const CommonRows& a, const smq::ScoreParams& s, cudaStream_t stream) {
+  smq::TopkParams t;
+  t.rows = a.rows;
+  t.topk = p->desc.topk;
+  t.topk_ld = a.topk_ld;
+  t.sbkv = p->sbkv;
+  t.nsb = p->nsb;
+  t.num_cols = p->num_cols;
+  t.logits = s.logits;
+  t.logits_fill = a.logits_out;
+  t.sparse_indices = a.sparse_indices;
+  t.end = a.end;
+  t.topk_out = a.topk_out;
+  t.col_indices = a.col_indices;
+  return smq::launch_topk(t, stream) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+int score_grid(const smq_plan* p, int rows) {
+  const int64_t max_tiles = static_cast<int64_t>(rows) * ((p->num_cols + kTileM - 1) / kTileM);
+  return static_cast<int>(max_tiles < p->num_sms ? max_tiles : p->num_sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+SMQ_API const char* smq_error_string(int code) {
+  switch (code) {
+    case SMQ_OK: return "ok";
+    case SMQ_ERR_INVALID_ARG: return "invalid argument";
+    case SMQ_ERR_UNSUPPORTED: return "unsupported geometry or device";
+    case SMQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SMQ_ERR_CUDA: return "CUDA error";
+    case SMQ_ERR_BOUNDS: return "device: index out of range";
+    case SMQ_ERR_TIMEOUT: return "device: pipeline wait timed out";
+    case SMQ_ERR_BOUNDS | SMQ_ERR_TIMEOUT: return "device: index out of range and pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+SMQ_API int smq_plan_create(const smq_plan_desc* desc, smq_plan** plan) {
+  if (!desc || !plan || desc->struct_size < sizeof(smq_plan_desc)) return SMQ_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const smq_plan_desc& d = *desc;
+  if (d.num_heads < 8 || d.num_heads > 128 || d.num_heads % 8 != 0) return SMQ_ERR_UNSUPPORTED;
+  if (d.head_dim != kHeadDim) return SMQ_ERR_UNSUPPORTED;
+  if (d.page_size <= 0 || d.candidate_block_size <= 0 || d.candidate_topk_blocks <= 0 || d.topk <= 0 ||
+      d.max_rows <= 0 || d.device < 0)
+    return SMQ_ERR_INVALID_ARG;
+  if (d.candidate_topk_blocks > 512 || d.max_rows > smq::kMaxRowsPerCall) return SMQ_ERR_UNSUPPORTED;
+  int sbkv = d.sparse_block_kv;
+  if (sbkv == 0) sbkv = pick_sbkv(d.page_size, d.candidate_block_size);
+  if (sbkv != 16 && sbkv != 32 && sbkv != 64 && sbkv != 128) return SMQ_ERR_UNSUPPORTED;
+  // the cache pages must be a multiple of the sub-block, and a candidate block splits into sub-blocks
+  if (d.page_size % sbkv != 0 || d.candidate_block_size % sbkv != 0) return SMQ_ERR_INVALID_ARG;
+  const int64_t nsb = static_cast<int64_t>(d.candidate_topk_blocks) * (d.candidate_block_size / sbkv);
+  const int64_t cols = nsb * sbkv;
+  if (cols > smq::kMaxSparseCols) return SMQ_ERR_UNSUPPORTED;
+  if (d.topk > cols) return SMQ_ERR_INVALID_ARG;  // the top-k must fit the sparse columns
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || d.device >= count) return SMQ_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d.device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d.device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess)
+    return SMQ_ERR_CUDA;
+  if (major != 10 || minor != 3) return SMQ_ERR_UNSUPPORTED;  // built for sm_103a only
+  smq_plan* p = new (std::nothrow) smq_plan;
+  if (!p) return SMQ_ERR_INVALID_ARG;
+  p->desc = d;
+  p->desc.sparse_block_kv = sbkv;
+  p->sbkv = sbkv;
+  p->nsb = static_cast<int32_t>(nsb);
+  p->num_cols = static_cast<int32_t>(cols);
+  p->page_bytes = d.page_size * (kHeadDim / 2 + kHeadDim / 32);
+  p->num_sms = sms;
+  p->n_mma = d.num_heads <= 64 ? 64 : 128;
+  p->prepared = false;
+  if (pick_stages(p, d.max_rows) == 0) {
+    delete p;
+    return SMQ_ERR_UNSUPPORTED;
+  }
+  *plan = p;
+  return SMQ_OK;
+}
+
+SMQ_API int smq_plan_destroy(smq_plan* plan) {
+  delete plan;
+  return SMQ_OK;
+}
+
+SMQ_API int smq_plan_get_info(const smq_plan* plan, smq_plan_info* info) {
+  if (!plan || !info || info->struct_size < sizeof(smq_plan_info)) return SMQ_ERR_INVALID_ARG;
+  info->sparse_block_kv = plan->sbkv;
+  info->num_sparse_blocks = plan->nsb;
+  info->num_sparse_cols = plan->num_cols;
+  info->page_bytes = plan->page_bytes;
+  info->num_sms = plan->num_sms;
+  return SMQ_OK;
+}
+
+SMQ_API int smq_workspace_size(const smq_plan* plan, int32_t rows, size_t* bytes) {
+  if (!plan || !bytes || rows < 0 || rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  *bytes = workspace_bytes_for(plan, rows);
+  return SMQ_OK;
+}
+
+SMQ_API int smq_workspace_init(const smq_plan* plan, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !workspace || workspace_bytes < kStatusBytes) return SMQ_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, kStatusBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SMQ_OK
+             : SMQ_ERR_CUDA;
+}
+
+SMQ_API int smq_get_status(const void* workspace, void* stream, int32_t* code) {
+  if (!workspace || !code) return SMQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SMQ_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (cudaMemset(const_cast<void*>(workspace), 0, sizeof v) != cudaSuccess) return SMQ_ERR_CUDA;
+  *code = v;
+  return SMQ_OK;
+}
+
+SMQ_API int sparse_mqa_candidate_expand(const smq_plan* plan, const int32_t* candidate_blocks,
+                                        const int32_t* row_ks, const int32_t* row_ke, int32_t rows,
+                                        int32_t* sparse_indices, int32_t* end, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!plan || rows < 0 || rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  if (rows == 0) return SMQ_OK;
+  if (!candidate_blocks || !row_ke || !sparse_indices || !end || !workspace) return SMQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kStatusBytes) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  int rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  return run_expand(plan, candidate_blocks, row_ks, row_ke, rows, sparse_indices, end,
+                    static_cast<cudaStream_t>(stream));
+}
+
+SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode_args* args, void* stream) {
+  if (!plan || !args || args->struct_size < sizeof(smq_decode_args)) return SMQ_ERR_INVALID_ARG;
+  const smq_decode_args& a = *args;
+  CommonRows c{a.rows, a.q, a.q_scale, a.weights, a.candidate_blocks, a.topk_out, a.topk_ld, a.sparse_indices,
+               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes};
+  int rc = check_common(plan, c);
+  if (rc != SMQ_OK || a.rows == 0) return rc;
+  if (!a.k_cache || !a.block_table || !a.row_ke || a.num_pages <= 0 || a.bt_rows <= 0 || a.bt_stride <= 0)
+    return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.k_cache, 32) || !aligned(a.block_table, 4)) return SMQ_ERR_INVALID_ARG;
+  rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int stages = pick_stages(plan, a.rows);
+  if (stages == 0) return SMQ_ERR_UNSUPPORTED;
+  CUtensorMap tm_q, tm_k;
+  rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
+  if (rc == SMQ_OK)
+    rc = encode_k_paged(&tm_k, a.k_cache, plan->desc.page_size, a.num_pages, plan->page_bytes, plan->sbkv);
+  if (rc != SMQ_OK) return rc;
+  record(a.profile_events[0], s);
+  if (!a.expansion_ready) {
+    rc = run_expand(plan, a.candidate_blocks, nullptr, a.row_ke, a.rows, a.sparse_indices, a.end, s);
+    if (rc != SMQ_OK) return rc;
+  }
+  record(a.profile_events[1], s);
+  smq::ScoreParams sp = score_params(plan, c, stages);
+  sp.k_cache = a.k_cache;
+  sp.num_pages = a.num_pages;
+  sp.page_bytes = plan->page_bytes;
+  sp.page_size = plan->desc.page_size;
+  sp.bt_rows = a.bt_rows;
+  sp.bt_stride = a.bt_stride;
+  sp.block_table = a.block_table;
+  sp.row_indices = a.row_indices;
+  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, plan->sbkv, stages, a.rows);
+  if (smq::launch_score_paged(sp, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess)
+    return SMQ_ERR_CUDA;
+  record(a.profile_events[2], s);
+  rc = run_topk(plan, c, sp, s);
+  record(a.profile_events[3], s);
+  return rc;
+}
+
+SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq_prefill_args* args,
+                                                 void* stream) {
+  if (!plan || !args || args->struct_size < sizeof(smq_prefill_args)) return SMQ_ERR_INVALID_ARG;
+  const smq_prefill_args& a = *args;
+  CommonRows c{a.rows, a.q, a.q_scale, a.weights, a.candidate_blocks, a.topk_out, a.topk_ld, a.sparse_indices,
+               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes};
+  int rc = check_common(plan, c);
+  if (rc != SMQ_OK || a.rows == 0) return rc;
+  if (!a.k_values || !a.k_scales || !a.cu_seqlen_ks || !a.cu_seqlen_ke || a.total_len <= 0 ||
+      a.total_len > (int64_t(1) << 31) - 1)
+    return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.k_values, 32) || !aligned(a.k_scales, 16)) return SMQ_ERR_INVALID_ARG;
+  rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int stages = pick_stages(plan, a.rows);
+  if (stages == 0) return SMQ_ERR_UNSUPPORTED;
+  CUtensorMap tm_q, tm_k, tm_ks;
+  rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
+  if (rc == SMQ_OK) rc = encode_k_contig(&tm_k, a.k_values, a.total_len, plan->sbkv);
+  if (rc == SMQ_OK) rc = encode_k_scales(&tm_ks, a.k_scales, a.total_len, plan->sbkv);
+  if (rc != SMQ_OK) return rc;
+  record(a.profile_events[0], s);
+  if (!a.expansion_ready) {
+    rc = run_expand(plan, a.candidate_blocks, a.cu_seqlen_ks, a.cu_seqlen_ke, a.rows, a.sparse_indices, a.end, s);
+    if (rc != SMQ_OK) return rc;
+  }
+  record(a.profile_events[1], s);
+  smq::ScoreParams sp = score_params(plan, c, stages);
+  sp.row_ks = a.cu_seqlen_ks;
+  sp.total_len = a.total_len;
+  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, plan->sbkv, stages, a.rows);
+  if (smq::launch_score_contig(sp, tm_q, tm_k, tm_ks, score_grid(plan, a.rows), smem, s) != cudaSuccess)
+    return SMQ_ERR_CUDA;
+  record(a.profile_events[2], s);
+  rc = run_topk(plan, c, sp, s);
+  record(a.profile_events[3], s);
+  return rc;
+}
+
+SMQ_API int sparse_mqa_gather_k(const smq_plan* plan, const uint8_t* k_cache, int64_t num_pages,
+                                const int32_t* block_table, int32_t bt_stride, const int32_t* cu_seq_lens,
+                                int32_t num_seqs, int64_t total_len, uint8_t* k_values, uint8_t* k_scales,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || num_seqs < 0 || total_len < 0) return SMQ_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_len == 0) return SMQ_OK;
+  if (!k_cache || !block_table || !cu_seq_lens || !k_values || !k_scales || !workspace || num_pages <= 0 ||
+      bt_stride <= 0)
+    return SMQ_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(k_values, 16) || !aligned(k_scales, 4)) return SMQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kStatusBytes) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  int rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  smq::GatherParams g;
+  g.num_seqs = num_seqs;
+  g.page_size = plan->desc.page_size;
+  g.bt_stride = bt_stride;
+  g.total_len = total_len;
+  g.num_pages = num_pages;
+  g.page_bytes = plan->page_bytes;
+  g.k_cache = k_cache;
+  g.block_table = block_table;
+  g.cu_seq_lens = cu_seq_lens;
+  g.k_values = k_values;
+  g.k_scales = k_scales;
+  g.status = static_cast<int32_t*>(workspace);
+  return smq::launch_gather(g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Kernel parameter blocks and launchers shared by the C ABI (smq_api.cu) and
+// the kernels (smq_kernels.cu). Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace smq {
+
+constexpr int kHeadDim = 128;       // D
+constexpr int kTileM = 128;         // key positions per MMA tile (the M of the MMA)
+constexpr int kRowBytes = 128;      // smem bytes per K row (padded FP4) and per Q row (E4M3)
+constexpr int kScaleWordBytes = 4;  // D/32 UE8M0 bytes per key position
+constexpr int kScoreThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int kTopkThreads = 512;
+constexpr int kExpandWarps = 8;
+constexpr int kMaxRowsPerCall = 16384;
+constexpr int kMaxSparseCols = 16384;
+constexpr int kStatusBounds = 8;    // SMQ_ERR_BOUNDS
+constexpr int kStatusTimeout = 16;  // SMQ_ERR_TIMEOUT
+
+// Everything the fused gather + score kernel reads besides its tensor maps.
+struct ScoreParams {
+  int32_t rows;
+  int32_t heads;          // H
+  int32_t n_mma;          // MMA N: H rounded up to 64 or 128
+  int32_t sbkv;           // tokens per sparse sub-block
+  int32_t subs_per_tile;  // kTileM / sbkv
+  int32_t nsb;            // sparse sub-blocks per row
+  int32_t num_cols;       // S = nsb * sbkv
+  int32_t stages;         // K pipeline depth
+  int32_t tmem_cols;      // TMEM columns allocated per CTA
+  const float* q_scale;
+  const uint16_t* weights;
+  const int32_t* sparse_indices;
+  const int32_t* end;
+  // paged cache (decode)
+  const uint8_t* k_cache;
+  int64_t num_pages;
+  int64_t page_bytes;
+  int32_t page_size;
+  int32_t bt_rows;
+  int32_t bt_stride;
+  const int32_t* block_table;
+  const int32_t* row_indices;  // may be null (identity)
+  // contiguous workspace (prefill)
+  const int32_t* row_ks;
+  int64_t total_len;
+  // outputs
+  float* logits;     // [rows][num_cols]
+  int32_t* status;   // workspace status word
+};
+
+struct TopkParams {
+  int32_t rows;
+  int32_t topk;
+  int32_t topk_ld;
+  int32_t sbkv;
+  int32_t nsb;
+  int32_t num_cols;
+  const float* logits;
+  float* logits_fill;  // when non-null: write -inf to columns >= end (the caller's logits_out)
+  const int32_t* sparse_indices;
+  const int32_t* end;
+  int32_t* topk_out;
+  int32_t* col_indices;  // may be null
+};
+
+struct ExpandParams {
+  int32_t rows;
+  int32_t ncb;
+  int32_t cbs;
+  int32_t sbkv;
+  int32_t nsb;
+  const int32_t* candidate_blocks;
+  const int32_t* row_ks;  // may be null
+  const int32_t* row_ke;
+  int32_t* sparse_indices;
+  int32_t* end;
+};
+
+struct GatherParams {
+  int32_t num_seqs;
+  int32_t page_size;
+  int32_t bt_stride;
+  int64_t total_len;
+  int64_t num_pages;
+  int64_t page_bytes;
+  const uint8_t* k_cache;
+  const int32_t* block_table;
+  const int32_t* cu_seq_lens;
+  uint8_t* k_values;
+  uint8_t* k_scales;
+  int32_t* status;
+};
+
+// Shared-memory bytes of the score kernel for a geometry.
+size_t score_smem_bytes(int n_mma, int heads, int sbkv, int stages, int rows);
+
+cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
+cudaError_t launch_score_paged(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
+                               size_t smem, cudaStream_t stream);
+cudaError_t launch_score_contig(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_ks, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
+
+}  // namespace smq

@@ -1,0 +1,204 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases compare every row against the dense oracle (score the whole
+context, mask, sort).  Full-size workloads compare every row's expansion
+and top-k structure, and the logits and top-k sets of many rows against the
+oracle's candidate-only mode (equal to the dense mode by the pinned
+invariant), in the launch configuration the benchmark times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_top_expand_gb300 as smq
+from sparse_attention_top_expand_gb300 import synth, tensors
+
+from gpu_check import check_rows, run_decode, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _ok(status):
+    assert status == 0, f"device status {status}"
+
+
+def test_tiny_decode_dense():
+    inp = synth.tiny_decode(0)
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
+
+
+GEOMS = [
+    # heads, page, cbs, ncb, topk, ctx range
+    (8, 64, 64, 6, 100, (1, 700)),
+    (16, 16, 32, 9, 40, (30, 900)),
+    (32, 32, 128, 5, 500, (100, 2000)),
+    (64, 128, 256, 4, 300, (1, 3000)),
+    (64, 64, 128, 16, 2048, (2048, 6000)),
+    (72, 64, 64, 8, 128, (64, 1100)),
+    (128, 64, 128, 7, 512, (1, 2500)),
+    (128, 32, 64, 12, 64, (500, 1500)),
+]
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"H{g[0]}-p{g[1]}-cbs{g[2]}-ncb{g[3]}-k{g[4]}")
+def test_decode_geometries_dense(geom):
+    h, page, cbs, ncb, topk, (lo, hi) = geom
+    rng = np.random.Generator(np.random.PCG64(h * 1000 + page + cbs))
+    rows = 12
+    ctx = rng.integers(lo, hi + 1, size=rows)
+    inp = synth._paged_decode(seed=h + page, rows=rows, h=h, page_size=page, cbs=cbs, ncb=ncb, topk=topk,
+                              ctx=ctx, row_perm=True)
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
+
+
+def test_decode_batch_full_size():
+    """64 rows, H=64, contexts 4096..32768, 32 blocks of 128, topk 2048."""
+    inp = synth.decode_batch()
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    ref = oracle.reference_rows(inp, mode="sparse")
+    check_rows(inp, dev, plan, ref)
+    dense = oracle.reference_rows(inp, rows=[0, 1], mode="dense")
+    check_rows(inp, dev, plan, dense, all_rows=False)
+
+
+def test_long_context_full_size():
+    """256 rows, contexts log-uniform to 131072, 10% shorter than topk."""
+    inp = synth.long_context_decode()
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    short = [r for r in range(inp.rows) if inp.row_ke[r] < inp.geom.topk]
+    sample = sorted(set(short[:12]) | set(range(0, inp.rows, 8)))
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, rows=sample, mode="sparse"))
+
+
+def test_prefill_small_dense():
+    inp = synth.prefill_chunk(seed=12, seq_lens=(1500, 2300, 700), queries_per_seq=40, num_heads=64,
+                              page_size=64, cbs=128, ncb=6, topk=300)
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    kv, ks = oracle.gather_reference(inp)
+    assert np.array_equal(tensors.to_numpy(dev.k_values), kv)
+    assert np.array_equal(tensors.to_numpy(dev.k_scales), ks)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
+
+
+def test_prefill_unaligned_sequence_starts():
+    """Sequence starts that are not multiples of 4 positions exercise the
+    scale loads that begin below the row and index past the remainder."""
+    inp = synth.prefill_chunk(seed=5, seq_lens=(1021, 999, 1502), queries_per_seq=24, num_heads=16,
+                              page_size=32, cbs=64, ncb=9, topk=200)
+    assert any(int(s) % 4 for s in inp.cu_seq_lens[1:-1])
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    kv, ks = oracle.gather_reference(inp)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
+
+
+def test_prefill_chunk_full_size():
+    """4096 rows from 2 sequences (28672 + 36864), causal ranges, topk 2048."""
+    inp = synth.prefill_chunk()
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    kv, ks = oracle.gather_reference(inp)
+    assert np.array_equal(tensors.to_numpy(dev.k_values), kv)
+    assert np.array_equal(tensors.to_numpy(dev.k_scales), ks)
+    sample = list(range(0, inp.rows, 61)) + [2047, 2048, 4095]
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, rows=sample, mode="sparse", contig=(kv, ks)))
+
+
+def test_shared_schedule_reuse_is_bit_identical():
+    """4 consumer layers share one expansion: reusing it gives the same bytes
+    as expanding inside every call."""
+    layers = synth.shared_schedule_layers(layers=4)
+    plan = tensors.plan_for(layers[0].geom, max_rows=layers[0].rows)
+    devs = [tensors.DecodeDevice(inp, plan) for inp in layers]
+    devs[0].expand(plan)
+    for d in devs[1:]:
+        d.sparse_indices.copy_(devs[0].sparse_indices)
+        d.end.copy_(devs[0].end)
+    for d in devs:
+        d.run(plan, expansion_ready=True)
+    fresh = [tensors.DecodeDevice(inp, plan) for inp in layers]
+    for d in fresh:
+        d.run(plan, expansion_ready=False)
+    for d in devs + fresh:
+        _ok(smq.smq_get_status(d.workspace))
+    for a, b in zip(devs, fresh):
+        assert torch.equal(a.topk_out, b.topk_out)
+        assert torch.equal(a.logits, b.logits)
+        assert torch.equal(a.sparse_indices, b.sparse_indices) and torch.equal(a.end, b.end)
+    for li, inp in enumerate(layers):
+        check_rows(inp, devs[li], plan, oracle.reference_rows(inp, rows=range(0, inp.rows, 9), mode="sparse"))
+
+
+def test_expand_golden_cases_on_gpu():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "expansion_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        page = c["sbkv"]
+        ncb = len(c["cand"])
+        plan = smq.Plan(num_heads=8, page_size=page, candidate_block_size=c["cbs"], candidate_topk_blocks=ncb,
+                        topk=1, max_rows=1, sparse_block_kv=c["sbkv"])
+        assert plan.num_sparse_blocks == c["nsb"] == ncb * c["cbs"] // c["sbkv"]
+        cand = torch.tensor([c["cand"]], dtype=torch.int32, device="cuda")
+        ke = torch.tensor([c["L"]], dtype=torch.int32, device="cuda")
+        si = torch.full((1, c["nsb"]), -7, dtype=torch.int32, device="cuda")
+        end = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        ws = plan.workspace(1)
+        smq.sparse_mqa_candidate_expand(plan, cand, None, ke, si, end, ws)
+        assert si.cpu().tolist()[0] == c["sparse_indices"], c["name"]
+        assert int(end.item()) == c["end"], c["name"]
+
+
+def test_ties_any_k_subset():
+    """Every key equal: all valid logits tie, any k of them is correct."""
+    inp = synth.tiny_decode(0)
+    inp.k_cache[:, : 64 * 64] = 0x22  # every element 1.0
+    inp.k_cache[:, 64 * 64:] = 127
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
+
+
+def test_zero_rows_is_a_no_op():
+    inp = synth.tiny_decode(0)
+    plan = tensors.plan_for(inp.geom, max_rows=4)
+    dev = tensors.DecodeDevice(inp, plan)
+    empty = torch.empty((0,) + tuple(dev.q.shape[1:]), dtype=torch.uint8, device=plan.device)
+    smq.sparse_mqa_logits_topk_decode(plan, empty, dev.q_scale[:0], dev.weights[:0], dev.k_cache, dev.block_table,
+                                      dev.row_indices[:0], dev.row_ke[:0], dev.candidate_blocks[:0],
+                                      dev.topk_out[:0], dev.sparse_indices[:0], dev.end[:0], dev.workspace)
+    torch.cuda.synchronize()
+    assert int((dev.topk_out == -7).sum()) == dev.topk_out.numel()
+
+
+def test_out_of_range_page_sets_bounds_status():
+    """A corrupt block-table entry is reported, not read."""
+    inp = synth.tiny_decode(0)
+    req = int(inp.row_indices[0])
+    b = int(inp.candidate_blocks[0][0])
+    inp.block_table[req][b] = inp.k_cache.shape[0] + 5
+    plan, dev, status = run_decode(inp)
+    assert status & smq.SMQ_ERR_BOUNDS
+    # rows that never touch the corrupt entry are unaffected
+    ref = oracle.reference_rows(inp, rows=[1, 2, 3], mode="dense")
+    check_rows(inp, dev, plan, ref, all_rows=False)
+
+
+def test_repeat_calls_are_deterministic():
+    inp = synth.decode_batch(rows=16)
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    first = (dev.topk_out.clone(), dev.logits.clone())
+    dev.run(plan)
+    _ok(smq.smq_get_status(dev.workspace))
+    assert torch.equal(first[0], dev.topk_out) and torch.equal(first[1], dev.logits)
