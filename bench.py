@@ -314,7 +314,7 @@ def run_ours(args, rank, world, dist):
 
     # graph of G steps, one pass over the replicas; per-step events inside it
     G = min(nrep, args.steps) if args.steps > 0 else 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
+    evs = [[timing_event(torch) for _ in range(4)] for _ in range(G)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for j in range(G):
@@ -360,7 +360,7 @@ def run_ours(args, rank, world, dist):
                 "topk": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
                 "source": f"CUDA events inside the timed graph, last replay ({G} launches)",
             }
-        except RuntimeError:
+        except (RuntimeError, ValueError):
             kernel_ms = eager_kernel_times(step, G, torch)
     for rep in reps:
         for d in rep:
@@ -417,9 +417,17 @@ def run_ours(args, rank, world, dist):
     return line
 
 
+def timing_event(torch):
+    """A timing CUDA event whose handle exists now: torch creates the driver
+    event on the first record(), and the library records it by handle."""
+    ev = torch.cuda.Event(enable_timing=True)
+    ev.record()
+    return ev
+
+
 def eager_kernel_times(step, n, torch):
     """Kernel durations from CUDA events on eager (uncaptured) calls."""
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    evs = [[timing_event(torch) for _ in range(4)] for _ in range(n)]
     for j in range(n):
         step(j, evs[j])
     torch.cuda.synchronize()

@@ -48,7 +48,7 @@
  *    positive and finite.
  *  - weights: [rows][H] bfloat16 (as uint16 bits).
  *  - Paged MXFP4 K cache: pages of page_size tokens. page_bytes =
- *    page_size * (D/2 + D/32), and the cache base must be 32-byte aligned.
+ *    page_size * (D/2 + D/32), and the cache base must be 16-byte aligned.
  *    A page is
  *      values [page_size][D/2]: OCP MX FP4 E2M1, element 2i in the low
  *        nibble of byte i and element 2i+1 in the high nibble;
@@ -103,7 +103,7 @@ typedef struct smq_plan_desc {
   int32_t topk;                  /* k: 1 <= k <= num_sparse_cols, k <= 16384 */
   int32_t sparse_block_kv;       /* sub-block size in tokens; 0 picks the largest of
                                     128/64/32/16 dividing both page_size and cbs */
-  int32_t max_rows;              /* upper bound on rows per call (workspace sizing) */
+  int32_t max_rows;              /* upper bound on rows per call (workspace sizing), <= 8192 */
   int32_t device;                /* CUDA device ordinal the plan runs on */
 } smq_plan_desc;
 
@@ -176,7 +176,7 @@ typedef struct smq_decode_args {
   const uint8_t *q;               /* device [R][H][D] E4M3 */
   const float *q_scale;           /* device [R] */
   const uint16_t *weights;        /* device [R][H] bf16 */
-  const uint8_t *k_cache;         /* device [num_pages][page_bytes], 32-byte aligned */
+  const uint8_t *k_cache;         /* device [num_pages][page_bytes], 16-byte aligned */
   int64_t num_pages;
   const int32_t *block_table;     /* device [bt_rows][bt_stride] page ids */
   int32_t bt_rows;
@@ -213,8 +213,8 @@ typedef struct smq_prefill_args {
   const uint8_t *q;               /* device [R][H][D] E4M3 */
   const float *q_scale;           /* device [R] */
   const uint16_t *weights;        /* device [R][H] bf16 */
-  const uint8_t *k_values;        /* device [total_len][D/2], 32-byte aligned */
-  const uint8_t *k_scales;        /* device [total_len][D/32], 16-byte aligned */
+  const uint8_t *k_values;        /* device [total_len][D/2], 16-byte aligned */
+  const uint8_t *k_scales;        /* device [total_len][D/32], 4-byte aligned */
   int64_t total_len;
   const int32_t *cu_seqlen_ks;    /* device [R] */
   const int32_t *cu_seqlen_ke;    /* device [R] */

@@ -67,53 +67,6 @@ int encode_q(CUtensorMap* m, const uint8_t* q, int64_t qrows, int n_mma) {
   return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
 }
 
-// Paged cache values: [num_pages][page_size][128 FP4] with page stride page_bytes,
-// unpacked on load to 16-byte containers (8 data bytes + 8 pad) for the MMA.
-int encode_k_paged(CUtensorMap* m, const uint8_t* cache, int page_size, int64_t num_pages, int64_t page_bytes,
-                   int sbkv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return SMQ_ERR_CUDA;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(page_size),
-                        static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim / 2), static_cast<cuuint64_t>(page_bytes)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(sbkv), 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(cache), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
-}
-
-// Contiguous workspace values [total_len][128 FP4], same unpacking.
-int encode_k_contig(CUtensorMap* m, const uint8_t* values, int64_t total_len, int sbkv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return SMQ_ERR_CUDA;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(total_len)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim / 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(sbkv)};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(values), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
-}
-
-// Contiguous workspace scales as one 32-bit word per position. A box of
-// sbkv + 4 words starts at a multiple of 4 positions so that every load
-// starts on a 16-byte boundary; the kernel indexes past the remainder.
-int encode_k_scales(CUtensorMap* m, const uint8_t* scales, int64_t total_len, int sbkv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return SMQ_ERR_CUDA;
-  cuuint64_t dims[1] = {static_cast<cuuint64_t>(total_len)};
-  cuuint64_t strides[1] = {0};
-  cuuint32_t box[1] = {static_cast<cuuint32_t>(sbkv + 4)};
-  cuuint32_t es[1] = {1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 1, const_cast<uint8_t*>(scales), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
-}
-
 constexpr size_t kStatusBytes = 256;
 
 size_t workspace_bytes_for(const smq_plan* p, int64_t rows) {
@@ -131,19 +84,9 @@ int check_device(smq_plan* p) {
   return SMQ_OK;
 }
 
-// Pipeline depth that fits the opt-in shared memory for this many rows.
-int pick_stages(const smq_plan* p, int rows) {
-  const size_t limit = 232448;
-  for (int st = 8; st >= 2; --st)
-    if (smq::score_smem_bytes(p->n_mma, p->desc.num_heads, p->sbkv, st, rows) <= limit) return st;
-  return 0;
-}
-
-int tmem_cols_for(int n_mma, int stages) {
-  const int need = 2 * n_mma + 4 * stages + 4;
-  int c = 32;
-  while (c < need) c <<= 1;
-  return c;
+// Whether the score kernel's shared memory fits the opt-in limit for this many rows.
+bool smem_fits(const smq_plan* p, int rows) {
+  return smq::score_smem_bytes(p->n_mma, p->desc.num_heads, rows) <= 232448;
 }
 
 // Record a caller's profiling event. Inside a stream capture it becomes an
@@ -189,7 +132,7 @@ int check_common(const smq_plan* p, const CommonRows& a) {
   return SMQ_OK;
 }
 
-smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a, int stages) {
+smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a) {
   smq::ScoreParams s;
   std::memset(&s, 0, sizeof s);
   s.rows = a.rows;
@@ -199,8 +142,7 @@ smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a, int stages
   s.subs_per_tile = kTileM / p->sbkv;
   s.nsb = p->nsb;
   s.num_cols = p->num_cols;
-  s.stages = stages;
-  s.tmem_cols = tmem_cols_for(p->n_mma, stages);
+  s.tmem_cols = smq::score_tmem_columns(p->n_mma);
   s.q_scale = a.q_scale;
   s.weights = a.weights;
   s.sparse_indices = a.sparse_indices;
@@ -305,7 +247,7 @@ SMQ_API int smq_plan_create(const smq_plan_desc* desc, smq_plan** plan) {
   p->num_sms = sms;
   p->n_mma = d.num_heads <= 64 ? 64 : 128;
   p->prepared = false;
-  if (pick_stages(p, d.max_rows) == 0) {
+  if (!smem_fits(p, d.max_rows)) {
     delete p;
     return SMQ_ERR_UNSUPPORTED;
   }
@@ -375,16 +317,13 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   if (rc != SMQ_OK || a.rows == 0) return rc;
   if (!a.k_cache || !a.block_table || !a.row_ke || a.num_pages <= 0 || a.bt_rows <= 0 || a.bt_stride <= 0)
     return SMQ_ERR_INVALID_ARG;
-  if (!aligned(a.k_cache, 32) || !aligned(a.block_table, 4)) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.k_cache, 16) || !aligned(a.block_table, 4)) return SMQ_ERR_INVALID_ARG;
   rc = check_device(const_cast<smq_plan*>(plan));
   if (rc != SMQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int stages = pick_stages(plan, a.rows);
-  if (stages == 0) return SMQ_ERR_UNSUPPORTED;
-  CUtensorMap tm_q, tm_k;
+  if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
+  CUtensorMap tm_q;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
-  if (rc == SMQ_OK)
-    rc = encode_k_paged(&tm_k, a.k_cache, plan->desc.page_size, a.num_pages, plan->page_bytes, plan->sbkv);
   if (rc != SMQ_OK) return rc;
   record(a.profile_events[0], s);
   if (!a.expansion_ready) {
@@ -392,7 +331,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
     if (rc != SMQ_OK) return rc;
   }
   record(a.profile_events[1], s);
-  smq::ScoreParams sp = score_params(plan, c, stages);
+  smq::ScoreParams sp = score_params(plan, c);
   sp.k_cache = a.k_cache;
   sp.num_pages = a.num_pages;
   sp.page_bytes = plan->page_bytes;
@@ -401,9 +340,8 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   sp.bt_stride = a.bt_stride;
   sp.block_table = a.block_table;
   sp.row_indices = a.row_indices;
-  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, plan->sbkv, stages, a.rows);
-  if (smq::launch_score_paged(sp, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess)
-    return SMQ_ERR_CUDA;
+  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
+  if (smq::launch_score(sp, true, tm_q, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);
@@ -421,16 +359,13 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
   if (!a.k_values || !a.k_scales || !a.cu_seqlen_ks || !a.cu_seqlen_ke || a.total_len <= 0 ||
       a.total_len > (int64_t(1) << 31) - 1)
     return SMQ_ERR_INVALID_ARG;
-  if (!aligned(a.k_values, 32) || !aligned(a.k_scales, 16)) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.k_values, 16) || !aligned(a.k_scales, 4)) return SMQ_ERR_INVALID_ARG;
   rc = check_device(const_cast<smq_plan*>(plan));
   if (rc != SMQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int stages = pick_stages(plan, a.rows);
-  if (stages == 0) return SMQ_ERR_UNSUPPORTED;
-  CUtensorMap tm_q, tm_k, tm_ks;
+  if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
+  CUtensorMap tm_q;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
-  if (rc == SMQ_OK) rc = encode_k_contig(&tm_k, a.k_values, a.total_len, plan->sbkv);
-  if (rc == SMQ_OK) rc = encode_k_scales(&tm_ks, a.k_scales, a.total_len, plan->sbkv);
   if (rc != SMQ_OK) return rc;
   record(a.profile_events[0], s);
   if (!a.expansion_ready) {
@@ -438,12 +373,13 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
     if (rc != SMQ_OK) return rc;
   }
   record(a.profile_events[1], s);
-  smq::ScoreParams sp = score_params(plan, c, stages);
+  smq::ScoreParams sp = score_params(plan, c);
   sp.row_ks = a.cu_seqlen_ks;
+  sp.k_values = a.k_values;
+  sp.k_scales = a.k_scales;
   sp.total_len = a.total_len;
-  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, plan->sbkv, stages, a.rows);
-  if (smq::launch_score_contig(sp, tm_q, tm_k, tm_ks, score_grid(plan, a.rows), smem, s) != cudaSuccess)
-    return SMQ_ERR_CUDA;
+  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
+  if (smq::launch_score(sp, false, tm_q, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);

@@ -11,18 +11,21 @@
 //
 // The score kernel is a persistent, warp-specialised pipeline with one CTA
 // per SM:
-//  - warp 0 (producer): for each 128-position tile it TMA-loads the FP4 key
-//    values of the tile's sub-blocks. A 16U4_ALIGN16B tensor map unpacks
-//    them into the padded layout the MMA reads, and per-position UE8M0 scales
-//    come in by bulk copy. When the row changes it also loads the row's Q tile
-//    (E4M3, 128-byte swizzle) and bf16 head weights.
+//  - warp 0 (scheduler): it resolves each 128-position tile's sub-blocks to
+//    source addresses (sparse id, block-table page, bounds) and publishes
+//    them per pipeline stage. When the row changes it TMA-loads the row's Q
+//    tile (E4M3, 128-byte swizzle) and bf16 head weights.
+//  - warps 6..9 (loaders): thread m owns key row m of every tile. It loads
+//    the row's 64 B of FP4 values and its UE8M0 scale word six tiles ahead,
+//    then stores the values into the padded 16-byte containers that
+//    kind::mxf8f6f4 reads for E2M1 (8 data bytes per 16 elements, 128-byte
+//    swizzle). It writes the scale word into TMEM, where row m of A reads
+//    lane m, column base + m/32, byte = scale id.
 //  - warp 1 (MMA): one thread issues 4 x tcgen05.mma kind::mxf8f6f4 with
 //    UE8M0 block scales, M = 128 positions, N = heads, K = 32 each. The
 //    accumulator (fp32) goes to TMEM, double-buffered.
-//  - warps 2..5 (epilogue): they write each tile's key scales into TMEM,
-//    where row m of A reads lane m, column base + m/32, byte = scale id.
-//    Then they read the accumulator, one TMEM lane (= one position) per
-//    thread, and reduce over heads with ReLU and the weights.
+//  - warps 2..5 (epilogue): one TMEM lane (= one position) per thread; they
+//    reduce over heads with ReLU and the weights.
 // Every wait is bounded. A wait that gives up sets SMQ_ERR_TIMEOUT in the
 // status word and the CTA winds down. Out-of-range page / row / block ids set
 // SMQ_ERR_BOUNDS, and the load is skipped.
@@ -41,33 +44,36 @@ constexpr uint32_t kE2M1 = 5, kE4M3 = 0;
 
 __host__ __device__ constexpr uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// One sub-block of a tile as the scheduler warp publishes it to the loaders.
+struct SubBlockSrc {
+  const uint8_t* values;  // FP4 values of its first position (64 B per position); null: not loaded
+  const uint8_t* scales;  // UE8M0 word of its first position (4 B per position)
+  int32_t positions;      // positions that may be read (fewer at the end of a contiguous workspace)
+  int32_t pad;
+};
+
 // Byte offsets inside the score kernel's dynamic shared memory (base aligned to 1024).
 struct ScoreLayout {
-  uint32_t kv, q, sf, sf_region, sf_stage, w, w_stride, meta, rem, bars, misc, scan, prefix, total;
-  __host__ __device__ ScoreLayout(int n_mma, int heads, int sbkv, int stages, int rows) {
+  uint32_t kv, q, desc, w, w_stride, meta, bars, misc, scan, prefix, total;
+  __host__ __device__ ScoreLayout(int n_mma, int heads, int rows) {
     uint32_t o = 0;
     kv = o;  // [stages][128 rows][128 B] padded FP4 keys, 128-byte swizzle
-    o += static_cast<uint32_t>(stages) * kTileM * kRowBytes;
+    o += static_cast<uint32_t>(kScoreStages) * kTileM * kRowBytes;
     q = o;  // [2][n_mma rows][128 B] E4M3 queries, 128-byte swizzle
     o += 2u * static_cast<uint32_t>(n_mma) * kRowBytes;
-    // one region per sub-block: sbkv + 4 scale words, 128-byte aligned (tensor-copy destination)
-    sf_region = round_up(static_cast<uint32_t>(sbkv + 4) * 4u, 128);
-    sf_stage = static_cast<uint32_t>(kTileM / sbkv) * sf_region;
-    sf = o;  // [stages][sub-blocks][sf_region bytes]
-    o += static_cast<uint32_t>(stages) * sf_stage;
+    desc = o;  // [stages][8 sub-blocks] source addresses published by the scheduler warp
+    o += static_cast<uint32_t>(kScoreStages) * 8u * sizeof(SubBlockSrc);
     w_stride = round_up(static_cast<uint32_t>(heads) * 2u, 16);
     w = o;  // [2][heads] bf16 weights
     o += 2u * w_stride;
-    meta = o;  // [2] {row, end, q_scale bits, unused}
+    meta = o;  // [2] {row, end, q_scale, unused}
     o += 2u * 16u;
-    rem = o;  // [stages] int: word offset of the first scale in the stage
-    o += round_up(static_cast<uint32_t>(stages) * 4u, 16);
-    bars = o;  // full, empty, sf_full [stages]; acc_full, acc_empty, q_full, q_empty [2]; drain
-    o += round_up((3u * static_cast<uint32_t>(stages) + 9u) * 8u, 16);
+    bars = o;  // desc_full, full, empty [stages]; acc_full, acc_empty [4]; q_full, q_empty [2]; drain [2]
+    o += round_up((3u * kScoreStages + 2u * kMaxAccBuffers + 6u) * 8u, 16);
     misc = o;  // tmem base, abort flag
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
-    o += 32u;
+    o += 64u;
     prefix = o;  // [rows + 1] exclusive prefix of tiles per row
     o += round_up((static_cast<uint32_t>(rows) + 1u) * 4u, 16);
     total = o;
@@ -101,8 +107,8 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) { atomicOr
 
 }  // namespace
 
-size_t score_smem_bytes(int n_mma, int heads, int sbkv, int stages, int rows) {
-  return ScoreLayout(n_mma, heads, sbkv, stages, rows).total + 1024;
+size_t score_smem_bytes(int n_mma, int heads, int rows) {
+  return ScoreLayout(n_mma, heads, rows).total + 1024;
 }
 
 // ===========================================================================
@@ -110,6 +116,8 @@ size_t score_smem_bytes(int n_mma, int heads, int sbkv, int stages, int rows) {
 // ===========================================================================
 __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_constant__ ExpandParams p) {
   extern __shared__ int32_t expand_smem[];
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kExpandWarps + warp;
   if (r >= p.rows) return;
@@ -121,10 +129,12 @@ __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_
   for (int i = lane; i < p.ncb; i += 32) cand[i] = p.candidate_blocks[static_cast<int64_t>(r) * p.ncb + i];
   __syncwarp();
   // keep a block if it is in range and its first occurrence; others -> INT_MAX
+  // (branch-free scans: every lane reads the same cand[j], a broadcast)
   for (int i = lane; i < p.ncb; i += 32) {
     const int32_t b = cand[i];
-    bool keep = b >= 0 && static_cast<int64_t>(b) * p.cbs < L;
-    for (int j = 0; keep && j < i; ++j) keep = cand[j] != b;
+    bool dup = false;
+    for (int j = 0; j < p.ncb; ++j) dup |= (j < i) & (cand[j] == b);
+    const bool keep = b >= 0 && static_cast<int64_t>(b) * p.cbs < L && !dup;
     kept[i] = keep ? b : INT_MAX;
   }
   __syncwarp();
@@ -161,56 +171,80 @@ __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_
 // ===========================================================================
 // Fused gather + score.
 // ===========================================================================
+// Global -> shared loads on the LSU path (the key rows of a tile come from
+// scattered pages; many independent 16-byte loads keep far more bytes in
+// flight per SM than the tensor-copy engine did for 64-byte rows).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 template <bool kPaged, int kN>
 __global__ void __launch_bounds__(kScoreThreads, 1)
-    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q,
-                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_ks) {
+    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ uint8_t score_smem_raw[];
   uint8_t* smem = align1024(score_smem_raw);
-  const ScoreLayout lay(kN, p.heads, p.sbkv, p.stages, p.rows);
+  const ScoreLayout lay(kN, p.heads, p.rows);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NS = p.stages;
+  constexpr int NS = kScoreStages;
   const int S = p.num_cols;
   const int R = p.rows;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
-  auto bar_full = [&](int s) { return smem_addr(&bars[s]); };
-  auto bar_empty = [&](int s) { return smem_addr(&bars[NS + s]); };
-  auto bar_sf = [&](int s) { return smem_addr(&bars[2 * NS + s]); };
+  auto bar_desc = [&](int s) { return smem_addr(&bars[s]); };
+  auto bar_full = [&](int s) { return smem_addr(&bars[NS + s]); };
+  auto bar_empty = [&](int s) { return smem_addr(&bars[2 * NS + s]); };
+  constexpr int NA = acc_buffers(kN);
   auto bar_acc_full = [&](int a) { return smem_addr(&bars[3 * NS + a]); };
-  auto bar_acc_empty = [&](int a) { return smem_addr(&bars[3 * NS + 2 + a]); };
-  auto bar_q_full = [&](int b) { return smem_addr(&bars[3 * NS + 4 + b]); };
-  auto bar_q_empty = [&](int b) { return smem_addr(&bars[3 * NS + 6 + b]); };
-  const uint32_t bar_drain = smem_addr(&bars[3 * NS + 8]);
+  auto bar_acc_empty = [&](int a) { return smem_addr(&bars[3 * NS + kMaxAccBuffers + a]); };
+  auto bar_q_full = [&](int b) { return smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + b]); };
+  auto bar_q_empty = [&](int b) { return smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + 2 + b]); };
+  const uint32_t bar_drain = smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + 4]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + lay.scan);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + lay.prefix);
   RowMeta* meta = reinterpret_cast<RowMeta*>(smem + lay.meta);
-  int32_t* stage_rem = reinterpret_cast<int32_t*>(smem + lay.rem);
+  SubBlockSrc* desc = reinterpret_cast<SubBlockSrc*>(smem + lay.desc);
 
   // ---- prologue: barriers, per-row tile counts and their prefix ---------
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full(s), 1);
+      mbar_init(bar_desc(s), 1);
+      mbar_init(bar_full(s), kLoaderThreads);
       mbar_init(bar_empty(s), 1);
-      mbar_init(bar_sf(s), 128);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NA; ++a) {
       mbar_init(bar_acc_full(a), 1);
-      mbar_init(bar_acc_empty(a), 128);
-      mbar_init(bar_q_full(a), 1);
-      mbar_init(bar_q_empty(a), 1 + 4);
+      mbar_init(bar_acc_empty(a), kEpilogueThreads);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_q_full(b), 1);
+      mbar_init(bar_q_empty(b), 2 + kEpilogueThreads / 32);  // both MMA issuers, the epilogue warps
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain + 8, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (tid == 32) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    if constexpr (!kPaged) prefetch_tmap(&tm_ks);
-  }
+  if (tid == 32 * kQueryWarp) prefetch_tmap(&tm_q);
+  // with programmatic dependent launch the prologue above overlaps the
+  // previous kernel; everything below reads what earlier kernels wrote
+  griddep_launch_dependents();
+  griddep_wait();
   const int per = (R + kScoreThreads - 1) / kScoreThreads;
   const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
   auto tiles_of = [&](int r) {
@@ -241,15 +275,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int n = static_cast<int>(t_end - t_begin);
   if (n <= 0) return;
 
-  // ---- TMEM: [acc 0 | acc 1 | SF-A per stage (4 cols) | SF-B (4 cols)] ----
+  // ---- TMEM: [acc 0 .. acc NA-1 | SF-A per stage (4 cols) | SF-B (4 cols)] ----
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_sfa = tmem + 2 * kN;
+  const uint32_t tm_sfa = tmem + NA * kN;
   const uint32_t tm_sfb = tm_sfa + 4 * NS;
-  if (warp >= 2) {  // B (query) scales are all 2^0
+  if (warp >= 2 && warp < 6) {  // B (query) scales are all 2^0
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     tmem_st4(tm_sfb + lane_base, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
     tmem_wait_st();
@@ -263,28 +297,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int H = p.heads;
 
   if (warp == 0) {
-    // ======================= producer =======================
+    // ======================= scheduler =======================
+    // Resolves each tile's sub-blocks to source addresses (row, sparse id,
+    // block-table page, bounds), publishes them per stage, and loads the
+    // row's query tile and weights when the row changes.
     const int tiles_per_batch = 32 / spt;
-    int cur_row = -1;
-    uint32_t quse = 0;
     int it = 0;
     bool ok = true;
     for (int64_t tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
-      // each lane resolves one sub-block of the batch
       const int64_t t = tb + lane / spt;
       const int sub = lane % spt;
-      int r = 0, e = 0, valid = 0, page = 0, tok = 0;
-      int64_t pos = 0;
-      float qs = 0.f;
+      int ntok = 0;
+      const uint8_t* vsrc = nullptr;
+      const uint8_t* ssrc = nullptr;
       if (t < t_end) {
-        r = find_row(prefix, R, t);
+        const int r = find_row(prefix, R, t);
         const int j = static_cast<int>(t - prefix[r]);
-        e = p.end[r];
+        int e = p.end[r];
         e = e < 0 ? 0 : (e > S ? S : e);
-        qs = p.q_scale[r];
         const int col_sub = j * spt + sub;
         if (col_sub * sbkv < e) {
           const int sb = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + col_sub];
+          bool valid = false;
           if (sb >= 0) {
             if constexpr (kPaged) {
               const int64_t tpos = static_cast<int64_t>(sb) * sbkv;
@@ -293,14 +327,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride) {
                 const int pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
                 if (pg >= 0 && pg < p.num_pages) {
-                  page = pg;
-                  tok = static_cast<int>(tpos % p.page_size);
-                  valid = 1;
+                  const int64_t tok = tpos % p.page_size;
+                  const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
+                  vsrc = base + tok * (kHeadDim / 2);
+                  ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+                  ntok = sbkv;
+                  valid = true;
                 }
               }
             } else {
-              pos = static_cast<int64_t>(p.row_ks[r]) + static_cast<int64_t>(sb) * sbkv;
-              valid = (pos >= 0 && pos < p.total_len) ? 1 : 0;
+              const int64_t pos = static_cast<int64_t>(p.row_ks[r]) + static_cast<int64_t>(sb) * sbkv;
+              if (pos >= 0 && pos < p.total_len) {
+                vsrc = p.k_values + pos * (kHeadDim / 2);
+                ssrc = p.k_scales + pos * kScaleWordBytes;
+                ntok = static_cast<int>(p.total_len - pos < sbkv ? p.total_len - pos : sbkv);
+                valid = true;
+              }
             }
           }
           if (!valid) set_status(p.status, kStatusBounds);
@@ -309,82 +351,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int k = 0; k < tiles_per_batch; ++k) {
         if (tb + k >= t_end) break;
         const int base = k * spt;
-        const int rk = __shfl_sync(kFullMask, r, base);
-        const int ek = __shfl_sync(kFullMask, e, base);
-        const float qsk = __shfl_sync(kFullMask, qs, base);
-        if (rk != cur_row) {
-          const int qb = quse & 1;
-          bool w_ok = true;
-          if (lane == 0) w_ok = mbar_wait(bar_q_empty(qb), ((quse >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
-          ok = __shfl_sync(kFullMask, w_ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          if (lane == 0) {
-            meta[qb].row = rk;
-            meta[qb].end = ek;
-            meta[qb].q_scale = qsk;
-            const uint32_t q_dst = smem_addr(smem + lay.q + qb * kN * kRowBytes);
-            const uint32_t w_dst = smem_addr(smem + lay.w + qb * lay.w_stride);
-            mbar_arrive_expect_tx(bar_q_full(qb), kN * kRowBytes + H * 2);
-            tma_load_2d(q_dst, &tm_q, 0, rk * H, bar_q_full(qb));
-            bulk_load(w_dst, p.weights + static_cast<int64_t>(rk) * H, H * 2, bar_q_full(qb));
-          }
-          cur_row = rk;
-          ++quse;
-        }
         const int s = it % NS;
         bool e_ok = true;
         if (lane == 0) e_ok = mbar_wait(bar_empty(s), ((it / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        // bytes this stage will receive
-        const uint32_t kv_stage = smem_addr(smem + lay.kv + s * (kTileM * kRowBytes));
-        const uint32_t sf_stage = smem_addr(smem + lay.sf + s * lay.sf_stage);
-        // tensor copies land on 128-byte boundaries (1024 for the swizzled keys); a
-        // destination that is not is reported and skipped instead of issued
-        auto dst_ok = [&](int u) {
-          return ((kv_stage + u * sbkv * kRowBytes) & 1023u) == 0 && ((sf_stage + u * lay.sf_region) & 127u) == 0;
-        };
-        uint32_t bytes = 0;
-        int rem = 0;
-        for (int u = 0; u < spt; ++u) {
-          const int v = __shfl_sync(kFullMask, valid, base + u);
-          const int64_t pu = __shfl_sync(kFullMask, pos, base + u);
-          if (v && !dst_ok(u)) {
-            if (lane == 0) set_status(p.status, kStatusBounds);
-          } else if (v) {
-            bytes += static_cast<uint32_t>(sbkv) * (kHeadDim / 2);  // packed FP4 bytes
-            if constexpr (kPaged) {
-              bytes += static_cast<uint32_t>(sbkv) * kScaleWordBytes;
-            } else {
-              bytes += static_cast<uint32_t>(sbkv + 4) * kScaleWordBytes;
-              rem = static_cast<int>(pu & 3);
-            }
-          }
+        // the lanes that resolved this tile's sub-blocks publish them
+        if (lane >= base && lane < base + spt) {
+          SubBlockSrc& d = desc[s * 8 + (lane - base)];
+          d.values = vsrc;
+          d.scales = ssrc;
+          d.positions = ntok;
         }
-        if (lane == 0) {
-          stage_rem[s] = rem;
-          mbar_arrive_expect_tx(bar_full(s), bytes);
-        }
-        for (int u = 0; u < spt; ++u) {
-          const int v = __shfl_sync(kFullMask, valid, base + u);
-          const int pg = __shfl_sync(kFullMask, page, base + u);
-          const int tk = __shfl_sync(kFullMask, tok, base + u);
-          const int64_t pu = __shfl_sync(kFullMask, pos, base + u);
-          if (lane == 0 && v && dst_ok(u)) {
-            const uint32_t kv_dst = kv_stage + u * sbkv * kRowBytes;
-            const uint32_t sf_dst = sf_stage + u * lay.sf_region;
-            if constexpr (kPaged) {
-              tma_load_3d(kv_dst, &tm_k, 0, tk, pg, bar_full(s));
-              const uint8_t* src = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes +
-                                   static_cast<int64_t>(p.page_size) * (kHeadDim / 2) +
-                                   static_cast<int64_t>(tk) * kScaleWordBytes;
-              bulk_load(sf_dst, src, sbkv * kScaleWordBytes, bar_full(s));
-            } else {
-              tma_load_2d(kv_dst, &tm_k, 0, static_cast<int32_t>(pu), bar_full(s));
-              tma_load_1d(sf_dst, &tm_ks, static_cast<int32_t>(pu & ~int64_t(3)), bar_full(s));
-            }
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_desc(s));
         ++it;
       }
     }
@@ -392,15 +372,56 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       set_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // let every load this warp issued land before the CTA exits
+    __syncwarp();
+  } else if (warp == kQueryWarp) {
+    // ======================= query loader =======================
+    // On every row change: wait until the row two back released its buffer,
+    // then TMA the row's Q tile and copy its bf16 weights; end and q_scale go
+    // along in shared memory. Kept apart from the scheduler so that address
+    // publishing never waits on a query buffer.
     if (lane == 0) {
-      const volatile int never = 0;
-      for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-        mbar_wait(bar_full(i % NS), (i / NS) & 1, &never, kWaitLimitNs);
+      int r = find_row(prefix, R, t_begin);
+      int cur = -1;
+      uint32_t quse = 0;
+      bool ok = true;
+      for (int it = 0; it < n && ok; ++it) {
+        const int64_t t = t_begin + it;
+        while (prefix[r + 1] <= t) ++r;
+        if (r == cur) continue;
+        cur = r;
+        const int qb = quse & 1;
+        ok = mbar_wait(bar_q_empty(qb), ((quse >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        int e = p.end[r];
+        meta[qb].row = r;
+        meta[qb].end = e < 0 ? 0 : (e > S ? S : e);
+        meta[qb].q_scale = p.q_scale[r];
+        const uint32_t q_dst = smem_addr(smem + lay.q + qb * kN * kRowBytes);
+        const uint32_t w_dst = smem_addr(smem + lay.w + qb * lay.w_stride);
+        mbar_arrive_expect_tx(bar_q_full(qb), kN * kRowBytes + H * 2);
+        tma_load_2d(q_dst, &tm_q, 0, r * H, bar_q_full(qb));
+        bulk_load(w_dst, p.weights + static_cast<int64_t>(r) * H, H * 2, bar_q_full(qb));
+        ++quse;
+      }
+      if (!ok) {
+        set_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // the last query load must land before the CTA exits (it has, unless a wait gave up)
+      if (quse > 0) {
+        const volatile int never = 0;
+        mbar_wait(bar_q_full((quse - 1) & 1), ((quse - 1) >> 1) & 1, &never, kWaitLimitNs);
+      }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ======================= MMA issuers =======================
+    // Issuing a tcgen05 instruction costs a thread ~100 cycles, so two
+    // threads share the work: warp 1 takes the even tiles, the other warp the
+    // odd ones. Each commits its own tiles' accumulators; at the end of every
+    // row both commit to the row's query buffer, which is free once the MMAs
+    // of both have finished.
+    const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
       uint32_t idesc[4];
       for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kTileM, kN, g, g);
@@ -414,105 +435,156 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (r != cur) {
           cur = r;
           qb = quse & 1;
-          ok = mbar_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, kWaitLimitNs);
           ++quse;
-          if (!ok) break;
         }
         const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1;
-        const int a = it & 1;
-        ok = mbar_wait(bar_full(s), ph, abort_flag, kWaitLimitNs) &&
-             mbar_wait(bar_sf(s), ph, abort_flag, kWaitLimitNs) &&
-             mbar_wait(bar_acc_empty(a), ((it >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t adesc = sw128_desc(smem_addr(smem + lay.kv + s * (kTileM * kRowBytes)));
-        const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q + qb * kN * kRowBytes));
-        for (int g = 0; g < 4; ++g)  // K = 32 per MMA; advance 32 bytes along the swizzled rows
-          mma_mxf8f6f4(tmem + a * kN, adesc + 2 * g, bdesc + 2 * g, idesc[g], tm_sfa + 4 * s, tm_sfb, g > 0);
-        mma_commit(bar_empty(s));
-        mma_commit(bar_acc_full(a));
+        if ((it & 1) == par) {
+          const int s = it % NS;
+          const int a = it % NA;
+          ok = mbar_wait(bar_q_full(qb), ((quse - 1) >> 1) & 1, abort_flag, kWaitLimitNs) &&
+               mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
+               mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t adesc = sw128_desc(smem_addr(smem + lay.kv + s * (kTileM * kRowBytes)));
+          const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q + qb * kN * kRowBytes));
+          for (int g = 0; g < 4; ++g)  // K = 32 per MMA; advance 32 bytes along the swizzled rows
+            mma_mxf8f6f4(tmem + a * kN, adesc + 2 * g, bdesc + 2 * g, idesc[g], tm_sfa + 4 * s, tm_sfb, g > 0);
+          mma_commit(bar_acc_full(a));
+        }
         if (last_of_row) mma_commit(bar_q_empty(qb));
       }
       if (!ok) {
         set_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
-      mma_commit(bar_drain);  // every MMA issued above has finished once this arrives
+      const uint32_t drain = bar_drain + 8 * par;
+      mma_commit(drain);  // every MMA this thread issued has finished once this arrives
       const volatile int never = 0;
-      mbar_wait(bar_drain, 0, &never, kWaitLimitNs);
+      mbar_wait(drain, 0, &never, kWaitLimitNs);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ======================= epilogue (warps 2..5) =======================
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q4 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    const int sub_of_m = m / sbkv, tok_of_m = m % sbkv;
     int r = find_row(prefix, R, t_begin);
     int cur = -1, qb = 0, row = 0, e = 0;
     uint32_t quse = 0;
     float qs = 0.f;
     float w[kN];
     bool ok = true;
-    for (int it = 0; it <= n && ok; ++it) {
-      if (it < n) {
-        // key scales of tile `it` into TMEM (row m reads lane m, column m / 32)
-        const int s = it % NS;
-        ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs);
+    for (int ie = 0; ie < n && ok; ++ie) {
+      const int64_t t = t_begin + ie;
+      while (prefix[r + 1] <= t) ++r;
+      if (r != cur) {
+        cur = r;
+        qb = quse & 1;
+        ok = warp_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, kWaitLimitNs);
+        ++quse;
         if (!ok) break;
-        const uint32_t* words = reinterpret_cast<const uint32_t*>(smem + lay.sf + s * lay.sf_stage);
-        const uint32_t word = words[sub_of_m * (lay.sf_region / 4) + stage_rem[s] + tok_of_m];
-        tmem_st1(tm_sfa + 4 * s + lane_base + q4, word);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar_sf(s));
+        row = meta[qb].row;
+        e = meta[qb].end;
+        qs = meta[qb].q_scale;
+        const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w + qb * lay.w_stride);
+#pragma unroll
+        for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
       }
-      if (it > 0) {
-        const int ie = it - 1;
-        const int64_t t = t_begin + ie;
-        while (prefix[r + 1] <= t) ++r;
-        if (r != cur) {
-          cur = r;
-          qb = quse & 1;
-          ok = mbar_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, kWaitLimitNs);
-          ++quse;
-          if (!ok) break;
-          row = meta[qb].row;
-          e = meta[qb].end;
-          qs = meta[qb].q_scale;
-          const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w + qb * lay.w_stride);
+      const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
+      const int a = ie % NA;
+      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
+      if (!ok) break;
+      // the MMAs of this tile have finished: its key stage and scale columns are free
+      if (warp == 2 && lane == 0) mbar_arrive(bar_empty(ie % NS));
+      tc_fence_after();
+      // four independent partial sums keep the FMA pipe busy instead of one
+      // 64-deep dependent chain
+      float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t tacc = tmem + a * kN + lane_base;
 #pragma unroll
-          for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+      for (int c = 0; c < kN; c += 32) {
+        uint32_t v0[16], v1[16];
+        tmem_ld16(tacc + c, v0);
+        tmem_ld16(tacc + c + 16, v1);
+        tmem_wait_ld();
+        if (c + 32 >= kN) {  // every column read: hand the accumulator back
+          tc_fence_before();
+          mbar_arrive(bar_acc_empty(a));
         }
-        const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
-        const int a = ie & 1;
-        ok = mbar_wait(bar_acc_full(a), (ie >> 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        tc_fence_after();
-        float acc = 0.f;
-        const uint32_t tacc = tmem + a * kN + lane_base;
 #pragma unroll
-        for (int c = 0; c < kN; c += 32) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tacc + c, v0);
-          tmem_ld16(tacc + c + 16, v1);
-          tmem_wait_ld();
-          if (c + 32 >= kN) {  // every column read: hand the accumulator back
-            tc_fence_before();
-            mbar_arrive(bar_acc_empty(a));
+        for (int h = 0; h < 16; ++h)
+          acc4[h & 3] = fmaf(w[c + h], fmaxf(__uint_as_float(v0[h]), 0.f), acc4[h & 3]);
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+          acc4[h & 3] = fmaf(w[c + 16 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc4[h & 3]);
+      }
+      const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+      const int col = static_cast<int>(t - prefix[r]) * kTileM + m;
+      if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
+      if (last_of_row) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_q_empty(qb));
+      }
+    }
+    if (!ok) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  } else if (warp >= 6 && warp < 10) {
+    // ======================= loaders (warps 6..9) =======================
+    // Thread m owns key row m of every tile: its 64 bytes of FP4 values and
+    // its 4-byte scale word, loaded kLoadAhead tiles before they are needed.
+    // The values are stored into the 16-byte containers the MMA reads (8
+    // data bytes per 16 elements, 128-byte swizzle); the scale word goes to
+    // TMEM lane m, column base + m/32.
+    const int q4 = warp & 3;
+    const int m = 32 * q4 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const int u = m / sbkv, tk = m % sbkv;
+    const uint32_t row_off = static_cast<uint32_t>(m) * kRowBytes;
+    const uint32_t swz = static_cast<uint32_t>(m & 7);
+    const uint32_t kv_base = smem_addr(smem + lay.kv);
+    uint4 v[kLoadAhead][4];
+    uint32_t sw[kLoadAhead];
+    bool have[kLoadAhead];
+#pragma unroll
+    for (int k = 0; k < kLoadAhead; ++k) have[k] = false;
+    bool ok = true;
+    for (int i0 = 0; i0 < n + kLoadAhead && ok; i0 += kLoadAhead) {
+#pragma unroll
+      for (int k = 0; k < kLoadAhead; ++k) {
+        const int i = i0 + k;
+        const int j = i - kLoadAhead;  // the tile whose data sits in slot k
+        if (j >= 0 && j < n) {
+          const int s = j % NS;
+          if (have[k]) {
+            const uint32_t dst = kv_base + s * (kTileM * kRowBytes) + row_off;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              sts_v2(dst + (((2 * c) ^ swz) << 4), v[k][c].x, v[k][c].y);
+              sts_v2(dst + (((2 * c + 1) ^ swz) << 4), v[k][c].z, v[k][c].w);
+            }
           }
-#pragma unroll
-          for (int h = 0; h < 16; ++h) acc = fmaf(w[c + h], fmaxf(__uint_as_float(v0[h]), 0.f), acc);
-#pragma unroll
-          for (int h = 0; h < 16; ++h) acc = fmaf(w[c + 16 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc);
+          fence_proxy_async_smem();  // make the stores visible to the tensor core's reads
+          tmem_st1(tm_sfa + 4 * s + lane_base + q4, sw[k]);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar_full(s));
         }
-        const int col = static_cast<int>(t - prefix[r]) * kTileM + m;
-        if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
-        if (last_of_row) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_q_empty(qb));
+        if (i < n) {
+          const int s = i % NS;
+          ok = warp_wait(bar_desc(s), (i / NS) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+          const SubBlockSrc d = desc[s * 8 + u];
+          have[k] = d.values != nullptr && tk < d.positions;
+          sw[k] = 0x7F7F7F7Fu;
+          if (have[k]) {
+            const uint8_t* src = d.values + static_cast<int64_t>(tk) * (kHeadDim / 2);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[k][c] = ldg_stream_v4(src + 16 * c);
+            sw[k] = ldg_stream_u32(d.scales + static_cast<int64_t>(tk) * kScaleWordBytes);
+          }
         }
       }
     }
@@ -534,23 +606,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // ===========================================================================
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
+// Thread t holds the keys of columns t, t + 512, t + 1024, ... in registers.
+// Three digit passes (11, 11, 10 bits, most significant first) build a
+// shared-memory histogram of the keys that still match the selected prefix;
+// a descending block scan over the bins finds the bin that holds the k-th
+// largest key. After the passes the threshold key T and the number of keys
+// equal to T to take are exact. One ordered compaction then writes every key
+// > T and the first `need` keys == T in column order.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+template <int kJ>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkParams p) {
-  extern __shared__ uint32_t topk_smem[];
   constexpr int kWarps = kTopkThreads / 32;
-  __shared__ int hist[256];
-  __shared__ int warp_a[kWarps], warp_b[kWarps];
-  __shared__ int sel_bin, sel_need;
+  constexpr int kBins = 2048;
+  extern __shared__ int32_t sidx[];  // [nsb] sparse sub-block ids of the row
+  __shared__ int hist[kBins];
+  __shared__ int wsum[kWarps];
+  __shared__ int wcnt[kWarps][kJ][2];
+  __shared__ int sel_bin, sel_above;
+  griddep_launch_dependents();
+  griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   const int S = p.num_cols;
   const int k = p.topk;
-  uint32_t* keys = topk_smem;
-  int32_t* sidx = reinterpret_cast<int32_t*>(topk_smem + S);
+  const int sbkv = p.sbkv;
   int e = p.end[r];
   e = e < 0 ? 0 : (e > S ? S : e);
   for (int i = tid; i < p.nsb; i += kTopkThreads) sidx[i] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + i];
@@ -558,9 +641,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     for (int c = e + tid; c < S; c += kTopkThreads) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
   int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
   int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * k : nullptr;
-  const int sbkv = p.sbkv;
-  __syncthreads();
   auto token = [&](int c) { return sidx[c / sbkv] * sbkv + c % sbkv; };
+  __syncthreads();
   if (e <= k) {
     for (int c = tid; c < k; c += kTopkThreads) {
       out[c] = c < e ? token(c) : -1;
@@ -569,71 +651,93 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     return;
   }
   const float* L = p.logits + static_cast<int64_t>(r) * S;
-  for (int c = tid; c < e; c += kTopkThreads) keys[c] = ordered_key(L[c]);
-  uint32_t prefix = 0;
-  int need = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+  uint32_t key[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int c = tid + j * kTopkThreads;
+    key[j] = c < e ? ordered_key(L[c]) : 0u;
+  }
+  uint32_t prefix = 0;  // selected high bits so far
+  int need = k;         // keys still to take among those matching the prefix
+  int done_bits = 0;
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int wbits = widths[pass];
+    const int shift = 32 - done_bits - wbits;
+    const int nb = 1 << wbits;
+    for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int c0 = 0; c0 < e; c0 += kTopkThreads) {
-      const int c = c0 + tid;
-      int bin = -1;
-      if (c < e) {
-        const uint32_t key = keys[c];
-        const bool match = pass == 0 || ((key ^ prefix) >> (shift + 8)) == 0;
-        if (match) bin = static_cast<int>((key >> shift) & 255u);
-      }
-      const uint32_t peers = __match_any_sync(kFullMask, bin);
-      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = tid + j * kTopkThreads;
+      const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
+      if (match) atomicAdd(&hist[(key[j] >> shift) & (nb - 1)], 1);
     }
     __syncthreads();
-    // inclusive scan over bins in descending order: thread i holds bin 255 - i
-    int cnt = tid < 256 ? hist[255 - tid] : 0;
-    int incl = cnt;
+    // descending scan: thread t owns bins nb-1-4t .. nb-4-4t (4 bins; fewer threads when nb = 1024)
+    int cnt[4];
+    int local = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int bin = nb - 1 - 4 * tid - b;
+      cnt[b] = bin >= 0 ? hist[bin] : 0;
+      local += cnt[b];
+    }
+    int incl = local;
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(kFullMask, incl, o);
       if (lane >= o) incl += v;
     }
-    if (lane == 31) warp_a[warp] = incl;
+    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    for (int w2 = 0; w2 < warp; ++w2) incl += warp_a[w2];
-    const int excl = incl - cnt;
-    if (tid < 256 && excl < need && need <= incl) {
-      sel_bin = 255 - tid;
-      sel_need = need - excl;
+    int cum = incl - local;
+    for (int w2 = 0; w2 < warp; ++w2) cum += wsum[w2];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if (cnt[b] > 0 && cum < need && need <= cum + cnt[b]) {
+        sel_bin = nb - 1 - 4 * tid - b;
+        sel_above = cum;
+      }
+      cum += cnt[b];
     }
     __syncthreads();
-    prefix |= static_cast<uint32_t>(sel_bin) << shift;
-    need = sel_need;
+    prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin);
+    need -= sel_above;
+    done_bits += wbits;
     __syncthreads();
   }
-  const uint32_t thr = prefix;  // key of the k-th largest logit
-  const int need_eq = need;     // how many keys equal to thr are selected
-  int base_gt = 0, base_eq = 0;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < e; c0 += kTopkThreads) {
-    const int c = c0 + tid;
-    const uint32_t key = c < e ? keys[c] : 0u;
-    const bool gt = c < e && key > thr;
-    const bool eq = c < e && key == thr;
-    const uint32_t bg = __ballot_sync(kFullMask, gt), be = __ballot_sync(kFullMask, eq);
+  const uint32_t thr = prefix;  // the k-th largest key
+  const int need_eq = need;     // keys equal to thr that are taken (in column order)
+  uint32_t bg[kJ], be[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int c = tid + j * kTopkThreads;
+    bg[j] = __ballot_sync(kFullMask, c < e && key[j] > thr);
+    be[j] = __ballot_sync(kFullMask, c < e && key[j] == thr);
     if (lane == 0) {
-      warp_a[warp] = __popc(bg);
-      warp_b[warp] = __popc(be);
+      wcnt[warp][j][0] = __popc(bg[j]);
+      wcnt[warp][j][1] = __popc(be[j]);
     }
-    __syncthreads();
-    int off_gt = base_gt, off_eq = base_eq, tot_gt = 0, tot_eq = 0;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  int gt_run = 0, eq_run = 0;  // counts in earlier chunks
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    int gt_before = gt_run, eq_before = eq_run, gt_tot = 0, eq_tot = 0;
     for (int w2 = 0; w2 < kWarps; ++w2) {
+      const int a = wcnt[w2][j][0], b = wcnt[w2][j][1];
       if (w2 < warp) {
-        off_gt += warp_a[w2];
-        off_eq += warp_b[w2];
+        gt_before += a;
+        eq_before += b;
       }
-      tot_gt += warp_a[w2];
-      tot_eq += warp_b[w2];
+      gt_tot += a;
+      eq_tot += b;
     }
-    const int pg = off_gt + __popc(bg & lt_mask);
-    const int pe = off_eq + __popc(be & lt_mask);
+    const int c = tid + j * kTopkThreads;
+    const bool gt = (bg[j] >> lane) & 1u, eq = (be[j] >> lane) & 1u;
+    const int pg = gt_before + __popc(bg[j] & lt);
+    const int pe = eq_before + __popc(be[j] & lt);
     int slot = -1;
     if (gt) slot = pg + min(pe, need_eq);
     else if (eq && pe < need_eq) slot = pg + pe;
@@ -641,9 +745,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       out[slot] = token(c);
       if (colo) colo[slot] = c;
     }
-    base_gt += tot_gt;
-    base_eq += tot_eq;
-    __syncthreads();
+    gt_run += gt_tot;
+    eq_run += eq_tot;
   }
 }
 
@@ -651,6 +754,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
 // Paged -> contiguous K gather: one thread per workspace row.
 // ===========================================================================
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t wrow = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (wrow >= p.total_len) return;
   int lo = 0, hi = p.num_seqs;
@@ -692,6 +797,21 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 cudaError_t prepare_kernels(int n_mma) {
   const int max_smem = 232448;  // 227 KB opt-in per block
   cudaError_t err;
+  // one shared-memory carveout for every kernel of a step, so that consecutive
+  // kernels never wait for the SM to re-split L1 and shared memory
+  const void* all[] = {reinterpret_cast<const void*>(&score_kernel<true, 64>),
+                       reinterpret_cast<const void*>(&score_kernel<false, 64>),
+                       reinterpret_cast<const void*>(&score_kernel<true, 128>),
+                       reinterpret_cast<const void*>(&score_kernel<false, 128>),
+                       reinterpret_cast<const void*>(&topk_kernel<8>),
+                       reinterpret_cast<const void*>(&topk_kernel<16>),
+                       reinterpret_cast<const void*>(&topk_kernel<32>),
+                       reinterpret_cast<const void*>(&expand_kernel),
+                       reinterpret_cast<const void*>(&gather_kernel)};
+  for (const void* f : all) {
+    err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+  }
   if (n_mma == 64) {
     err = cudaFuncSetAttribute(score_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
@@ -702,48 +822,71 @@ cudaError_t prepare_kernels(int n_mma) {
     err = cudaFuncSetAttribute(score_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   }
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (kMaxSparseCols + kMaxSparseCols / 16) * 4);
-  if (err != cudaSuccess) return err;
+
   return cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kExpandWarps * 2 * 512 * 4);
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes; it waits (griddepcontrol.wait)
+// before touching anything an earlier kernel wrote.
+template <typename P>
+cudaError_t launch_pdl(void (*kernel)(P), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       const P& params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
+template <typename P, typename Q>
+cudaError_t launch_pdl2(void (*kernel)(P, Q), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                        const P& a, const Q& b) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, b);
 }
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
   const int grid = (p.rows + kExpandWarps - 1) / kExpandWarps;
   const size_t smem = static_cast<size_t>(kExpandWarps) * 2 * p.ncb * sizeof(int32_t);
-  expand_kernel<<<grid, kExpandWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(expand_kernel, grid, kExpandWarps * 32, smem, stream, p);
 }
 
-cudaError_t launch_score_paged(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
-                               size_t smem, cudaStream_t stream) {
-  if (p.n_mma == 64)
-    score_kernel<true, 64><<<grid, kScoreThreads, smem, stream>>>(p, tm_q, tm_k, tm_k);
-  else
-    score_kernel<true, 128><<<grid, kScoreThreads, smem, stream>>>(p, tm_q, tm_k, tm_k);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_score_contig(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                const CUtensorMap& tm_ks, int grid, size_t smem, cudaStream_t stream) {
-  if (p.n_mma == 64)
-    score_kernel<false, 64><<<grid, kScoreThreads, smem, stream>>>(p, tm_q, tm_k, tm_ks);
-  else
-    score_kernel<false, 128><<<grid, kScoreThreads, smem, stream>>>(p, tm_q, tm_k, tm_ks);
-  return cudaGetLastError();
+cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
+                         cudaStream_t stream) {
+  if (paged)
+    return p.n_mma == 64 ? launch_pdl2(score_kernel<true, 64>, grid, kScoreThreads, smem, stream, p, tm_q)
+                         : launch_pdl2(score_kernel<true, 128>, grid, kScoreThreads, smem, stream, p, tm_q);
+  return p.n_mma == 64 ? launch_pdl2(score_kernel<false, 64>, grid, kScoreThreads, smem, stream, p, tm_q)
+                       : launch_pdl2(score_kernel<false, 128>, grid, kScoreThreads, smem, stream, p, tm_q);
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(p.num_cols + p.nsb) * 4;
-  topk_kernel<<<p.rows, kTopkThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  const size_t smem = static_cast<size_t>(p.nsb) * 4;
+  if (p.num_cols <= 8 * kTopkThreads) return launch_pdl(topk_kernel<8>, p.rows, kTopkThreads, smem, stream, p);
+  if (p.num_cols <= 16 * kTopkThreads) return launch_pdl(topk_kernel<16>, p.rows, kTopkThreads, smem, stream, p);
+  return launch_pdl(topk_kernel<32>, p.rows, kTopkThreads, smem, stream, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
   const int64_t blocks = (p.total_len + 255) / 256;
-  gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, static_cast<unsigned>(blocks), 256, 0, stream, p);
 }
 
 }  // namespace smq

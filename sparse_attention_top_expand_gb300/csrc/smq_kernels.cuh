@@ -14,10 +14,25 @@ constexpr int kHeadDim = 128;       // D
 constexpr int kTileM = 128;         // key positions per MMA tile (the M of the MMA)
 constexpr int kRowBytes = 128;      // smem bytes per K row (padded FP4) and per Q row (E4M3)
 constexpr int kScaleWordBytes = 4;  // D/32 UE8M0 bytes per key position
-constexpr int kScoreThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int kScoreThreads = 384;  // scheduler, 2 MMA, 4 epilogue, 4 loader and 1 query-loader warps
+constexpr int kQueryWarp = 10;
+constexpr int kMmaWarp1 = 11;       // second MMA issuer (odd tiles); warp 1 issues the even tiles
+constexpr int kEpilogueThreads = 128;
+constexpr int kLoaderThreads = 128;
+constexpr int kScoreStages = 8;     // key tiles resident in shared memory
+constexpr int kLoadAhead = 6;       // tiles each loader thread keeps in flight (< kScoreStages)
+constexpr int kMaxAccBuffers = 4;
+
+// TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 3 x 128 fp32 columns.
+__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 3; }
+
+// TMEM columns per CTA: accumulators, then 4 scale columns per stage, then 4 for the query scales.
+__host__ __device__ constexpr int score_tmem_columns(int n_mma) {
+  return acc_buffers(n_mma) * n_mma + 4 * kScoreStages + 4 <= 256 ? 256 : 512;
+}
 constexpr int kTopkThreads = 512;
 constexpr int kExpandWarps = 8;
-constexpr int kMaxRowsPerCall = 16384;
+constexpr int kMaxRowsPerCall = 8192;
 constexpr int kMaxSparseCols = 16384;
 constexpr int kStatusBounds = 8;    // SMQ_ERR_BOUNDS
 constexpr int kStatusTimeout = 16;  // SMQ_ERR_TIMEOUT
@@ -31,7 +46,6 @@ struct ScoreParams {
   int32_t subs_per_tile;  // kTileM / sbkv
   int32_t nsb;            // sparse sub-blocks per row
   int32_t num_cols;       // S = nsb * sbkv
-  int32_t stages;         // K pipeline depth
   int32_t tmem_cols;      // TMEM columns allocated per CTA
   const float* q_scale;
   const uint16_t* weights;
@@ -48,6 +62,8 @@ struct ScoreParams {
   const int32_t* row_indices;  // may be null (identity)
   // contiguous workspace (prefill)
   const int32_t* row_ks;
+  const uint8_t* k_values;
+  const uint8_t* k_scales;
   int64_t total_len;
   // outputs
   float* logits;     // [rows][num_cols]
@@ -98,13 +114,11 @@ struct GatherParams {
 };
 
 // Shared-memory bytes of the score kernel for a geometry.
-size_t score_smem_bytes(int n_mma, int heads, int sbkv, int stages, int rows);
+size_t score_smem_bytes(int n_mma, int heads, int rows);
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
-cudaError_t launch_score_paged(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
-                               size_t smem, cudaStream_t stream);
-cudaError_t launch_score_contig(const ScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                const CUtensorMap& tm_ks, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
+                         cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device

@@ -18,6 +18,18 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// -------------------------------------------------- dependent grid launch
+
+// Let the next kernel of the stream launch (its CTAs still wait, in
+// griddep_wait, for this grid to finish before touching its outputs).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on have finished and their writes
+// are visible. A no-op for a normal launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -40,25 +52,41 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.b32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(100000u)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete. Gives up after
-// `limit_ns` or as soon as *abort becomes non-zero; returns false then.
+// `limit_ns` or once *abort becomes non-zero; returns false then. The clock and
+// the abort flag are read only every 256 polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > limit_ns) return false;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit_ns) return false;
+    }
   }
+}
+
+// The same wait for a whole warp: lane 0 polls, the warp then resumes together
+// (__syncwarp orders the other lanes after lane 0's acquire).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
 }
 
 // ------------------------------------------------------------ async copies
