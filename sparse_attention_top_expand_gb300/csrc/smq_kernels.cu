@@ -61,15 +61,16 @@ struct ScoreLayout {
     o += static_cast<uint32_t>(kScoreStages) * kTileM * kRowBytes;
     q = o;  // [2][n_mma rows][128 B] E4M3 queries, 128-byte swizzle
     o += 2u * static_cast<uint32_t>(n_mma) * kRowBytes;
-    desc = o;  // [stages][8 sub-blocks] source addresses published by the scheduler warp
-    o += static_cast<uint32_t>(kScoreStages) * 8u * sizeof(SubBlockSrc);
+    desc = o;  // [ring][8 sub-blocks] source addresses published by the scheduler warp
+    o += static_cast<uint32_t>(kDescRing) * 8u * sizeof(SubBlockSrc);
     w_stride = round_up(static_cast<uint32_t>(heads) * 2u, 16);
     w = o;  // [2][heads] bf16 weights
     o += 2u * w_stride;
     meta = o;  // [2] {row, end, q_scale, unused}
     o += 2u * 16u;
-    bars = o;  // desc_full, full, empty [stages]; acc_full, acc_empty [4]; q_full, q_empty [2]; drain [2]
-    o += round_up((3u * kScoreStages + 2u * kMaxAccBuffers + 6u) * 8u, 16);
+    bars = o;  // full, empty [stages]; acc_full, acc_empty [4]; q_full, q_empty [2]; drain [2];
+               // desc_full, desc_empty [ring]
+    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing) * 8u, 16);
     misc = o;  // tmem base, abort flag
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
@@ -204,15 +205,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int R = p.rows;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
-  auto bar_desc = [&](int s) { return smem_addr(&bars[s]); };
-  auto bar_full = [&](int s) { return smem_addr(&bars[NS + s]); };
-  auto bar_empty = [&](int s) { return smem_addr(&bars[2 * NS + s]); };
+  auto bar_full = [&](int s) { return smem_addr(&bars[s]); };
+  auto bar_empty = [&](int s) { return smem_addr(&bars[NS + s]); };
   constexpr int NA = acc_buffers(kN);
-  auto bar_acc_full = [&](int a) { return smem_addr(&bars[3 * NS + a]); };
-  auto bar_acc_empty = [&](int a) { return smem_addr(&bars[3 * NS + kMaxAccBuffers + a]); };
-  auto bar_q_full = [&](int b) { return smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + b]); };
-  auto bar_q_empty = [&](int b) { return smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + 2 + b]); };
-  const uint32_t bar_drain = smem_addr(&bars[3 * NS + 2 * kMaxAccBuffers + 4]);
+  constexpr int NB = 2 * NS + 2 * kMaxAccBuffers;
+  auto bar_acc_full = [&](int a) { return smem_addr(&bars[2 * NS + a]); };
+  auto bar_acc_empty = [&](int a) { return smem_addr(&bars[2 * NS + kMaxAccBuffers + a]); };
+  auto bar_q_full = [&](int b) { return smem_addr(&bars[NB + b]); };
+  auto bar_q_empty = [&](int b) { return smem_addr(&bars[NB + 2 + b]); };
+  const uint32_t bar_drain = smem_addr(&bars[NB + 4]);
+  auto bar_desc_full = [&](int d) { return smem_addr(&bars[NB + 6 + d]); };
+  auto bar_desc_empty = [&](int d) { return smem_addr(&bars[NB + 6 + kDescRing + d]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + lay.scan);
@@ -223,9 +226,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // ---- prologue: barriers, per-row tile counts and their prefix ---------
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_desc(s), 1);
       mbar_init(bar_full(s), kLoaderThreads);
       mbar_init(bar_empty(s), 1);
+    }
+    for (int d = 0; d < kDescRing; ++d) {
+      mbar_init(bar_desc_full(d), 1);
+      mbar_init(bar_desc_empty(d), kLoaderThreads / 32);
     }
     for (int a = 0; a < NA; ++a) {
       mbar_init(bar_acc_full(a), 1);
@@ -351,20 +357,23 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int k = 0; k < tiles_per_batch; ++k) {
         if (tb + k >= t_end) break;
         const int base = k * spt;
-        const int s = it % NS;
+        // publish into the address ring; it does not wait for pipeline stages,
+        // only for the loaders to have read the entry published kDescRing tiles ago
+        const int dslot = it % kDescRing;
         bool e_ok = true;
-        if (lane == 0) e_ok = mbar_wait(bar_empty(s), ((it / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (lane == 0)
+          e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the lanes that resolved this tile's sub-blocks publish them
         if (lane >= base && lane < base + spt) {
-          SubBlockSrc& d = desc[s * 8 + (lane - base)];
+          SubBlockSrc& d = desc[dslot * 8 + (lane - base)];
           d.values = vsrc;
           d.scales = ssrc;
           d.positions = ntok;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_desc(s));
+        if (lane == 0) mbar_arrive(bar_desc_full(dslot));
         ++it;
       }
     }
@@ -558,6 +567,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int j = i - kLoadAhead;  // the tile whose data sits in slot k
         if (j >= 0 && j < n) {
           const int s = j % NS;
+          // the stage is free once the MMAs of tile j - NS have finished
+          ok = warp_wait(bar_empty(s), ((j / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
           if (have[k]) {
             const uint32_t dst = kv_base + s * (kTileM * kRowBytes) + row_off;
 #pragma unroll
@@ -573,10 +585,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           mbar_arrive(bar_full(s));
         }
         if (i < n) {
-          const int s = i % NS;
-          ok = warp_wait(bar_desc(s), (i / NS) & 1, abort_flag, kWaitLimitNs);
+          const int dslot = i % kDescRing;
+          ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
-          const SubBlockSrc d = desc[s * 8 + u];
+          const SubBlockSrc d = desc[dslot * 8 + u];
+          __syncwarp();  // every lane has read the entry before it is handed back
+          if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
           have[k] = d.values != nullptr && tk < d.positions;
           sw[k] = 0x7F7F7F7Fu;
           if (have[k]) {

@@ -22,6 +22,7 @@ constexpr int kLoaderThreads = 128;
 constexpr int kScoreStages = 8;     // key tiles resident in shared memory
 constexpr int kLoadAhead = 6;       // tiles each loader thread keeps in flight (< kScoreStages)
 constexpr int kMaxAccBuffers = 4;
+constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 
 // TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 3 x 128 fp32 columns.
 __host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 3; }
