@@ -202,6 +202,33 @@ typedef struct smq_decode_args {
 SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan *plan, const smq_decode_args *args,
                                           void *stream);
 
+/* Paged decode for callers that cannot allocate device memory, for
+ * example code running where cudaMalloc is forbidden or where memory is
+ * owned by another allocator (a graph-replay engine or a runtime that hands
+ * out only its own tensors). The pages have no counterpart to this call.
+ *
+ * It does what sparse_mqa_logits_topk_decode does, with the same arguments,
+ * except that args->workspace must be NULL and args->workspace_bytes 0. The
+ * library uses its own scratch instead: a static device array of 256 bytes
+ * plus 8 MiB (SMQ_NOALLOC_SCRATCH_BYTES) for the fp32 logits, held on every
+ * GPU that loads the library until the process exits.
+ *  - Rows * num_sparse_cols * 4 must not exceed 8 MiB, for example 256 rows
+ *    of 8192 columns. A larger call returns SMQ_ERR_WORKSPACE_TOO_SMALL and
+ *    enqueues nothing.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current. Make that first call
+ *    before any stream capture.
+ *  - Every call shares the one scratch: calls that overlap on the GPU (on
+ *    different streams without ordering) race. Each call zeroes the scratch
+ *    status word first.
+ *  - Device-detected errors (bad page or row ids, timeouts) are recorded in
+ *    the scratch and not returned. Callers who need them use
+ *    sparse_mqa_logits_topk_decode with a workspace.
+ * It calls no cudaMalloc, cudaFree or allocating routine. */
+#define SMQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan *plan, const smq_decode_args *args,
+                                                  void *stream);
+
 /* One prefill chunk on a contiguous K workspace. (Source: sparse_mqa_indexer
  * docs, SparseMQAIndexer.forward, the sparse_mqa_logits_prefill_chunk call
  * with cu_seqlen_ks / cu_seqlen_ke.) Row r's keys are workspace rows

@@ -27,6 +27,7 @@ SMQ_ERR_WORKSPACE_TOO_SMALL = 3
 SMQ_ERR_CUDA = 4
 SMQ_ERR_BOUNDS = 8
 SMQ_ERR_TIMEOUT = 16
+SMQ_NOALLOC_SCRATCH_BYTES = 8 << 20  # logits scratch of sparse_mqa_logits_topk_decode_noalloc
 
 _c_i32 = ctypes.c_int32
 _c_u32 = ctypes.c_uint32
@@ -66,7 +67,7 @@ class SMQPrefillArgs(ctypes.Structure):
 EXPORTED = [
     "smq_plan_create", "smq_plan_destroy", "smq_plan_get_info", "smq_workspace_size", "smq_workspace_init",
     "smq_get_status", "smq_error_string", "sparse_mqa_candidate_expand", "sparse_mqa_logits_topk_decode",
-    "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k",
+    "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k", "sparse_mqa_logits_topk_decode_noalloc",
 ]
 
 _lib = None
@@ -91,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.smq_error_string.restype = ctypes.c_char_p
     lib.sparse_mqa_candidate_expand.argtypes = [_vp, _vp, _vp, _vp, _c_i32, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.sparse_mqa_logits_topk_decode.argtypes = [_vp, P(SMQDecodeArgs), _vp]
+    lib.sparse_mqa_logits_topk_decode_noalloc.argtypes = [_vp, P(SMQDecodeArgs), _vp]
     lib.sparse_mqa_logits_topk_prefill_chunk.argtypes = [_vp, P(SMQPrefillArgs), _vp]
     lib.sparse_mqa_gather_k.argtypes = [_vp, _vp, _c_i64, _vp, _c_i32, _vp, _c_i32, _c_i64, _vp, _vp, _vp,
                                         ctypes.c_size_t, _vp]
@@ -262,6 +264,39 @@ def sparse_mqa_logits_topk_decode(plan: Plan, q, q_scale, weights, k_cache, bloc
     _set_events(a, profile_events)
     _check(load_library().sparse_mqa_logits_topk_decode(plan.handle, ctypes.byref(a), _stream(stream)),
            "sparse_mqa_logits_topk_decode")
+
+
+def sparse_mqa_logits_topk_decode_noalloc(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices,
+                                          row_ke, candidate_blocks, topk_out, sparse_indices, end,
+                                          expansion_ready: bool = False, col_indices=None, logits_out=None,
+                                          stream=None) -> None:
+    """Paged decode on the library's static scratch: no workspace argument,
+    at most 8 MiB of fp32 logits (rows x sparse columns), calls must not
+    overlap on the GPU, device-detected errors are not reported."""
+    dev = plan.device
+    a = SMQDecodeArgs()
+    a.struct_size = ctypes.sizeof(SMQDecodeArgs)
+    a.rows = int(q.shape[0])
+    a.q = _ptr(q, _U8, "q", dev)
+    a.q_scale = _ptr(q_scale, _F32, "q_scale", dev)
+    a.weights = _ptr(weights, _BF16, "weights", dev)
+    a.k_cache = _ptr(k_cache, _U8, "k_cache", dev)
+    a.num_pages = int(k_cache.shape[0])
+    a.block_table = _ptr(block_table, _I32, "block_table", dev)
+    a.bt_rows = int(block_table.shape[0])
+    a.bt_stride = int(block_table.shape[1])
+    a.row_indices = _ptr(row_indices, _I32, "row_indices", dev)
+    a.row_ke = _ptr(row_ke, _I32, "row_ke", dev)
+    a.candidate_blocks = _ptr(candidate_blocks, _I32, "candidate_blocks", dev)
+    a.topk_out = _ptr(topk_out, _I32, "topk_out", dev)
+    a.topk_ld = int(topk_out.shape[1])
+    a.sparse_indices = _ptr(sparse_indices, _I32, "sparse_indices", dev)
+    a.end = _ptr(end, _I32, "end", dev)
+    a.expansion_ready = 1 if expansion_ready else 0
+    a.col_indices = _ptr(col_indices, _I32, "col_indices", dev)
+    a.logits_out = _ptr(logits_out, _F32, "logits_out", dev)
+    _check(load_library().sparse_mqa_logits_topk_decode_noalloc(plan.handle, ctypes.byref(a), _stream(stream)),
+           "sparse_mqa_logits_topk_decode_noalloc")
 
 
 def sparse_mqa_logits_topk_prefill_chunk(plan: Plan, q, q_scale, weights, k_values, k_scales, cu_seqlen_ks,

@@ -193,6 +193,38 @@ int score_grid(const smq_plan* p, int rows) {
 
 }  // namespace
 
+// Scratch of sparse_mqa_logits_topk_decode_noalloc: a status header, then
+// the fp32 logits. Some callers cannot hand the library a workspace: a
+// runtime whose device memory all belongs to its own pool and is not lent
+// out, or a plugin that may touch only the buffers it was handed. For them the scratch is part of the
+// loaded module, one copy on every device the library is loaded on. Only the
+// status word must start at zero (each call clears it); the score kernel
+// writes every logits column it covers before top-k reads it.
+static __device__ __align__(256) uint8_t smq_noalloc_scratch[kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch on device `dev`, which must be current. In
+// host code the array's name is only a stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device.
+int noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SMQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, smq_noalloc_scratch) != cudaSuccess || !p) return SMQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SMQ_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 SMQ_API const char* smq_error_string(int code) {
@@ -413,6 +445,28 @@ SMQ_API int sparse_mqa_gather_k(const smq_plan* plan, const uint8_t* k_cache, in
   g.k_scales = k_scales;
   g.status = static_cast<int32_t*>(workspace);
   return smq::launch_gather(g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const smq_decode_args* args,
+                                                  void* stream) {
+  if (!plan || !args || args->struct_size < sizeof(smq_decode_args)) return SMQ_ERR_INVALID_ARG;
+  if (args->workspace || args->workspace_bytes) return SMQ_ERR_INVALID_ARG;  // the library's scratch replaces it
+  if (args->rows < 0 || args->rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  const size_t logits_bytes = static_cast<size_t>(args->rows) * plan->num_cols * sizeof(float);
+  if (logits_bytes > SMQ_NOALLOC_SCRATCH_BYTES) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  if (args->rows == 0) return SMQ_OK;
+  int rc = check_device(const_cast<smq_plan*>(plan));  // the plan's device is current
+  if (rc != SMQ_OK) return rc;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(plan->desc.device, &scratch);
+  if (rc != SMQ_OK) return rc;
+  // the kernels OR device-detected errors into the status word: start it at zero
+  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMQ_ERR_CUDA;
+  smq_decode_args a = *args;
+  a.workspace = scratch;
+  a.workspace_bytes = kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES;
+  return sparse_mqa_logits_topk_decode(plan, &a, stream);
 }
 
 }  // extern "C"
