@@ -15,15 +15,17 @@
 //    source addresses (sparse id, block-table page, bounds) and publishes
 //    them per pipeline stage. When the row changes it TMA-loads the row's Q
 //    tile (E4M3, 128-byte swizzle) and bf16 head weights.
-//  - warps 6..9 (loaders): thread m owns key row m of every tile. It loads
-//    the row's 64 B of FP4 values and its UE8M0 scale word six tiles ahead,
-//    then stores the values into the padded 16-byte containers that
+//  - warps 6..9 (loaders): they load each tile's FP4 values in 512-byte
+//    coalesced warp loads and its UE8M0 scale words six tiles ahead, then
+//    store the values into the padded 16-byte containers that
 //    kind::mxf8f6f4 reads for E2M1 (8 data bytes per 16 elements, 128-byte
-//    swizzle). It writes the scale word into TMEM, where row m of A reads
-//    lane m, column base + m/32, byte = scale id.
-//  - warp 1 (MMA): one thread issues 4 x tcgen05.mma kind::mxf8f6f4 with
-//    UE8M0 block scales, M = 128 positions, N = heads, K = 32 each. The
-//    accumulator (fp32) goes to TMEM, double-buffered.
+//    swizzle). Thread m writes the scale word of key row m into the stage's
+//    512-byte scale block in shared memory.
+//  - warps 1 and 11 (MMA, even and odd tiles): one thread copies the stage's
+//    scale block to TMEM (tcgen05.cp; row m of A reads lane m, column
+//    base + m/32, byte = scale id) and issues 4 x tcgen05.mma kind::mxf8f6f4
+//    with UE8M0 block scales, M = 128 positions, N = heads, K = 32 each. The
+//    fp32 accumulators live in TMEM, several in flight.
 //  - warps 2..5 (epilogue): one TMEM lane (= one position) per thread; they
 //    reduce over heads with ReLU and the weights.
 // Every wait is bounded. A wait that gives up sets SMQ_ERR_TIMEOUT in the
@@ -54,13 +56,15 @@ struct SubBlockSrc {
 
 // Byte offsets inside the score kernel's dynamic shared memory (base aligned to 1024).
 struct ScoreLayout {
-  uint32_t kv, q, desc, w, w_stride, meta, bars, misc, scan, prefix, total;
+  uint32_t kv, q, sf, desc, w, w_stride, meta, bars, misc, scan, prefix, total;
   __host__ __device__ ScoreLayout(int n_mma, int heads, int rows) {
     uint32_t o = 0;
     kv = o;  // [stages][128 rows][128 B] padded FP4 keys, 128-byte swizzle
     o += static_cast<uint32_t>(kScoreStages) * kTileM * kRowBytes;
     q = o;  // [2][n_mma rows][128 B] E4M3 queries, 128-byte swizzle
     o += 2u * static_cast<uint32_t>(n_mma) * kRowBytes;
+    sf = o;  // [stages][32 rows][16 B] key scale words, copied to TMEM by the MMA thread; then one block of 2^0
+    o += static_cast<uint32_t>(kScoreStages + 1) * 512u;
     desc = o;  // [ring][8 sub-blocks] source addresses published by the scheduler warp
     o += static_cast<uint32_t>(kDescRing) * 8u * sizeof(SubBlockSrc);
     w_stride = round_up(static_cast<uint32_t>(heads) * 2u, 16);
@@ -69,8 +73,8 @@ struct ScoreLayout {
     meta = o;  // [2] {row, end, q_scale, unused}
     o += 2u * 16u;
     bars = o;  // full, empty [stages]; acc_full, acc_empty [4]; q_full, q_empty [2]; drain [2];
-               // desc_full, desc_empty [ring]
-    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing) * 8u, 16);
+               // desc_full, desc_empty [ring]; setup copy
+    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing + 1u) * 8u, 16);
     misc = o;  // tmem base, abort flag
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
@@ -189,8 +193,38 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t a) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+// The address ring is shared between warps that hand entries back and forth
+// through mbarriers. Its reads and writes are volatile shared accesses, so
+// that the compiler neither delays them past the hand-off nor repeats a read
+// after the entry has been handed back and rewritten.
+__device__ __forceinline__ void put_src(SubBlockSrc* e, const uint8_t* values, const uint8_t* scales, int positions) {
+  const uint32_t a = smem_addr(e);
+  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a), "l"(values) : "memory");
+  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a + 8), "l"(scales) : "memory");
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(a + 16), "r"(positions) : "memory");
+}
+
+__device__ __forceinline__ SubBlockSrc get_src(const SubBlockSrc* e) {
+  const uint32_t a = smem_addr(e);
+  uint64_t v, sc;
+  int32_t n;
+  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(sc) : "r"(a + 8) : "memory");
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(n) : "r"(a + 16) : "memory");
+  SubBlockSrc d;
+  d.values = reinterpret_cast<const uint8_t*>(v);
+  d.scales = reinterpret_cast<const uint8_t*>(sc);
+  d.positions = n;
+  d.pad = 0;
+  return d;
 }
 
 template <bool kPaged, int kN>
@@ -216,6 +250,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t bar_drain = smem_addr(&bars[NB + 4]);
   auto bar_desc_full = [&](int d) { return smem_addr(&bars[NB + 6 + d]); };
   auto bar_desc_empty = [&](int d) { return smem_addr(&bars[NB + 6 + kDescRing + d]); };
+  const uint32_t bar_setup = smem_addr(&bars[NB + 6 + 2 * kDescRing]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + lay.scan);
@@ -243,6 +278,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain + 8, 1);
+    mbar_init(bar_setup, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -289,10 +325,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_sfa = tmem + NA * kN;
   const uint32_t tm_sfb = tm_sfa + 4 * NS;
-  if (warp >= 2 && warp < 6) {  // B (query) scales are all 2^0
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    tmem_st4(tm_sfb + lane_base, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    tmem_wait_st();
+  // B (query) scales are all 2^0: one 512-byte block of 0x7F copied to the
+  // SF-B columns by the first MMA thread, complete before any MMA is issued
+  uint32_t* sf_one = reinterpret_cast<uint32_t*>(smem + lay.sf + kScoreStages * 512);
+  if (tid < 128) sf_one[tid] = 0x7F7F7F7Fu;
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 32) {
+    tmem_cp_32x128b_x4(tm_sfb, rows16_desc(smem_addr(sf_one)));
+    mma_commit(bar_setup);
+    if (!mbar_wait(bar_setup, 0, abort_flag, kWaitLimitNs)) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -319,17 +364,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (t < t_end) {
         const int r = find_row(prefix, R, t);
         const int j = static_cast<int>(t - prefix[r]);
-        int e = p.end[r];
-        e = e < 0 ? 0 : (e > S ? S : e);
         const int col_sub = j * spt + sub;
-        if (col_sub * sbkv < e) {
-          const int sb = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + col_sub];
+        // the row's end, sparse id and block-table row do not depend on each
+        // other: issue the three loads together
+        const bool in_row = col_sub < p.nsb;
+        int e = p.end[r];
+        const int sb = in_row ? p.sparse_indices[static_cast<int64_t>(r) * p.nsb + col_sub] : -1;
+        const int brow = kPaged ? (p.row_indices ? p.row_indices[r] : r) : 0;
+        e = e < 0 ? 0 : (e > S ? S : e);
+        if (in_row && col_sub * sbkv < e) {
           bool valid = false;
           if (sb >= 0) {
             if constexpr (kPaged) {
               const int64_t tpos = static_cast<int64_t>(sb) * sbkv;
               const int64_t slot = tpos / p.page_size;
-              const int brow = p.row_indices ? p.row_indices[r] : r;
               if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride) {
                 const int pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
                 if (pg >= 0 && pg < p.num_pages) {
@@ -366,12 +414,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the lanes that resolved this tile's sub-blocks publish them
-        if (lane >= base && lane < base + spt) {
-          SubBlockSrc& d = desc[dslot * 8 + (lane - base)];
-          d.values = vsrc;
-          d.scales = ssrc;
-          d.positions = ntok;
-        }
+        if (lane >= base && lane < base + spt) put_src(&desc[dslot * 8 + (lane - base)], vsrc, ssrc, ntok);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_desc_full(dslot));
         ++it;
@@ -455,6 +498,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
+          // the stage's key scales: shared memory -> TMEM, in order before the MMAs below
+          tmem_cp_32x128b_x4(tm_sfa + 4 * s, rows16_desc(smem_addr(smem + lay.sf + s * 512)));
           const uint64_t adesc = sw128_desc(smem_addr(smem + lay.kv + s * (kTileM * kRowBytes)));
           const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q + qb * kN * kRowBytes));
           for (int g = 0; g < 4; ++g)  // K = 32 per MMA; advance 32 bytes along the swizzled rows
@@ -542,23 +587,31 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   } else if (warp >= 6 && warp < 10) {
     // ======================= loaders (warps 6..9) =======================
-    // Thread m owns key row m of every tile: its 64 bytes of FP4 values and
-    // its 4-byte scale word, loaded kLoadAhead tiles before they are needed.
-    // The values are stored into the 16-byte containers the MMA reads (8
-    // data bytes per 16 elements, 128-byte swizzle); the scale word goes to
-    // TMEM lane m, column base + m/32.
+    // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
+    // t / 4 + 32 k (k = 0..3), so that each warp load reads 512 contiguous
+    // bytes (8 rows of one sub-block). Scale words: thread t owns key row t.
+    // Both are loaded kLoadAhead tiles before they are needed. The values are
+    // stored into the 16-byte containers the MMA reads (8 data bytes per 16
+    // elements, 128-byte swizzle); the scale word goes to TMEM lane t, column
+    // base + t/32.
     const int q4 = warp & 3;
     const int m = 32 * q4 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    const int u = m / sbkv, tk = m % sbkv;
-    const uint32_t row_off = static_cast<uint32_t>(m) * kRowBytes;
-    const uint32_t swz = static_cast<uint32_t>(m & 7);
+    const uint32_t sf_base = smem_addr(smem + lay.sf);
+    const int vch = m & 3;
+    int vu[4], vtk[4];
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int pos = (m >> 2) + 32 * k4;
+      vu[k4] = pos / sbkv;
+      vtk[k4] = pos % sbkv;
+    }
+    const int su = m / sbkv, stk = m % sbkv;
     const uint32_t kv_base = smem_addr(smem + lay.kv);
     uint4 v[kLoadAhead][4];
     uint32_t sw[kLoadAhead];
-    bool have[kLoadAhead];
+    uint32_t have[kLoadAhead];  // bit k4: value chunk k4 was loaded
 #pragma unroll
-    for (int k = 0; k < kLoadAhead; ++k) have[k] = false;
+    for (int k = 0; k < kLoadAhead; ++k) have[k] = 0;
     bool ok = true;
     for (int i0 = 0; i0 < n + kLoadAhead && ok; i0 += kLoadAhead) {
 #pragma unroll
@@ -570,35 +623,44 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // the stage is free once the MMAs of tile j - NS have finished
           ok = warp_wait(bar_empty(s), ((j / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
-          if (have[k]) {
-            const uint32_t dst = kv_base + s * (kTileM * kRowBytes) + row_off;
+          const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              sts_v2(dst + (((2 * c) ^ swz) << 4), v[k][c].x, v[k][c].y);
-              sts_v2(dst + (((2 * c + 1) ^ swz) << 4), v[k][c].z, v[k][c].w);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            if (have[k] & (1u << k4)) {
+              const int pos = (m >> 2) + 32 * k4;
+              const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
+              const uint32_t swz = static_cast<uint32_t>(pos & 7);
+              sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k4].x, v[k][k4].y);
+              sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k4].z, v[k][k4].w);
             }
           }
+          // scale word of key row m: word 4 (m % 32) + m / 32 of the stage's block,
+          // which the copy to TMEM places at lane m, column base + m / 32
+          sts_u32(sf_base + s * 512 + 16 * lane + 4 * q4, sw[k]);
           fence_proxy_async_smem();  // make the stores visible to the tensor core's reads
-          tmem_st1(tm_sfa + 4 * s + lane_base + q4, sw[k]);
-          tmem_wait_st();
-          tc_fence_before();
           mbar_arrive(bar_full(s));
         }
         if (i < n) {
           const int dslot = i % kDescRing;
           ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
-          const SubBlockSrc d = desc[dslot * 8 + u];
+          const SubBlockSrc* dring = desc + dslot * 8;
+          uint32_t hv = 0;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const SubBlockSrc d = get_src(dring + vu[k4]);
+            if (d.values != nullptr && vtk[k4] < d.positions) {
+              v[k][k4] = ldg_stream_v4(d.values + static_cast<int64_t>(vtk[k4]) * (kHeadDim / 2) + 16 * vch);
+              hv |= 1u << k4;
+            }
+          }
+          have[k] = hv;
+          sw[k] = 0x7F7F7F7Fu;
+          const SubBlockSrc ds = get_src(dring + su);
+          if (ds.values != nullptr && stk < ds.positions)
+            sw[k] = ldg_stream_u32(ds.scales + static_cast<int64_t>(stk) * kScaleWordBytes);
           __syncwarp();  // every lane has read the entry before it is handed back
           if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
-          have[k] = d.values != nullptr && tk < d.positions;
-          sw[k] = 0x7F7F7F7Fu;
-          if (have[k]) {
-            const uint8_t* src = d.values + static_cast<int64_t>(tk) * (kHeadDim / 2);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[k][c] = ldg_stream_v4(src + 16 * c);
-            sw[k] = ldg_stream_u32(d.scales + static_cast<int64_t>(tk) * kScaleWordBytes);
-          }
         }
       }
     }
@@ -621,12 +683,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
 // Thread t holds the keys of columns t, t + 512, t + 1024, ... in registers.
-// Three digit passes (11, 11, 10 bits, most significant first) build a
+// Up to three digit passes (11, 11, 10 bits, most significant first) build a
 // shared-memory histogram of the keys that still match the selected prefix;
 // a descending block scan over the bins finds the bin that holds the k-th
-// largest key. After the passes the threshold key T and the number of keys
-// equal to T to take are exact. One ordered compaction then writes every key
-// > T and the first `need` keys == T in column order.
+// largest key. The passes stop early once every key of the selected bin is
+// taken. Then every key above the selected prefix, and the first `need` keys
+// inside it in column order, are written by one ordered compaction: a single
+// scan over the per-32-column counts gives each warp its output offsets.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -636,11 +699,12 @@ template <int kJ>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkParams p) {
   constexpr int kWarps = kTopkThreads / 32;
   constexpr int kBins = 2048;
-  extern __shared__ int32_t sidx[];  // [nsb] sparse sub-block ids of the row
-  __shared__ int hist[kBins];
+  constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
+  extern __shared__ int32_t sidx[];     // [nsb] sparse sub-block ids of the row
+  __shared__ int hist[2][kBins];
   __shared__ int wsum[kWarps];
-  __shared__ int wcnt[kWarps][kJ][2];
-  __shared__ int sel_bin, sel_above;
+  __shared__ uint32_t chunk_cnt[kChunks];  // (above << 16) | inside, then their exclusive prefix
+  __shared__ int sel_bin[3], sel_above[3], sel_cnt[3];
   griddep_launch_dependents();
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -648,9 +712,18 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   const int S = p.num_cols;
   const int k = p.topk;
   const int sbkv = p.sbkv;
+  const float* L = p.logits + static_cast<int64_t>(r) * S;
+  // the logits row has S columns whatever `end` is: load every key at once
+  float raw[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int c = tid + j * kTopkThreads;
+    raw[j] = c < S ? L[c] : 0.f;
+  }
   int e = p.end[r];
   e = e < 0 ? 0 : (e > S ? S : e);
   for (int i = tid; i < p.nsb; i += kTopkThreads) sidx[i] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + i];
+  for (int i = tid; i < kBins; i += kTopkThreads) hist[0][i] = 0;
   if (p.logits_fill)
     for (int c = e + tid; c < S; c += kTopkThreads) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
   int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
@@ -664,13 +737,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     }
     return;
   }
-  const float* L = p.logits + static_cast<int64_t>(r) * S;
   uint32_t key[kJ];
 #pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const int c = tid + j * kTopkThreads;
-    key[j] = c < e ? ordered_key(L[c]) : 0u;
-  }
+  for (int j = 0; j < kJ; ++j) key[j] = tid + j * kTopkThreads < e ? ordered_key(raw[j]) : 0u;
   uint32_t prefix = 0;  // selected high bits so far
   int need = k;         // keys still to take among those matching the prefix
   int done_bits = 0;
@@ -679,22 +748,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     const int wbits = widths[pass];
     const int shift = 32 - done_bits - wbits;
     const int nb = 1 << wbits;
-    for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
+    int* h = hist[pass & 1];
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int c = tid + j * kTopkThreads;
       const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
-      if (match) atomicAdd(&hist[(key[j] >> shift) & (nb - 1)], 1);
+      if (match) atomicAdd(&h[(key[j] >> shift) & (nb - 1)], 1);
     }
     __syncthreads();
+    // the other buffer was last read before the previous pass's second barrier
+    for (int i = tid; i < kBins; i += kTopkThreads) hist[(pass + 1) & 1][i] = 0;
     // descending scan: thread t owns bins nb-1-4t .. nb-4-4t (4 bins; fewer threads when nb = 1024)
     int cnt[4];
     int local = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const int bin = nb - 1 - 4 * tid - b;
-      cnt[b] = bin >= 0 ? hist[bin] : 0;
+      cnt[b] = bin >= 0 ? h[bin] : 0;
       local += cnt[b];
     }
     int incl = local;
@@ -705,53 +775,67 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     int cum = incl - local;
-    for (int w2 = 0; w2 < warp; ++w2) cum += wsum[w2];
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) cum += w2 < warp ? wsum[w2] : 0;  // independent loads
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       if (cnt[b] > 0 && cum < need && need <= cum + cnt[b]) {
-        sel_bin = nb - 1 - 4 * tid - b;
-        sel_above = cum;
+        sel_bin[pass] = nb - 1 - 4 * tid - b;
+        sel_above[pass] = cum;
+        sel_cnt[pass] = cnt[b];
       }
       cum += cnt[b];
     }
     __syncthreads();
-    prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin);
-    need -= sel_above;
+    prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin[pass]);
+    need -= sel_above[pass];
     done_bits += wbits;
-    __syncthreads();
+    if (need == sel_cnt[pass]) break;  // the whole bin is taken
   }
-  const uint32_t thr = prefix;  // the k-th largest key
-  const int need_eq = need;     // keys equal to thr that are taken (in column order)
+  // selected: keys whose top done_bits bits are above the prefix, and the
+  // first `need` of those equal to it, in column order
+  const uint32_t mask = ~0u << (32 - done_bits);
+  const uint32_t pfx = prefix << (32 - done_bits);
+  const int need_eq = need;
   uint32_t bg[kJ], be[kJ];
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
     const int c = tid + j * kTopkThreads;
-    bg[j] = __ballot_sync(kFullMask, c < e && key[j] > thr);
-    be[j] = __ballot_sync(kFullMask, c < e && key[j] == thr);
-    if (lane == 0) {
-      wcnt[warp][j][0] = __popc(bg[j]);
-      wcnt[warp][j][1] = __popc(be[j]);
+    bg[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) > pfx);
+    be[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) == pfx);
+    if (lane == 0) chunk_cnt[j * kWarps + warp] = (static_cast<uint32_t>(__popc(bg[j])) << 16) | __popc(be[j]);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the packed counts (each half stays below 2^16)
+    constexpr int kPer = kChunks / 32;
+    uint32_t v[kPer];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      v[i] = chunk_cnt[lane * kPer + i];
+      sum += v[i];
+    }
+    uint32_t inc = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += t;
+    }
+    uint32_t run = inc - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      chunk_cnt[lane * kPer + i] = run;
+      run += v[i];
     }
   }
   __syncthreads();
   const uint32_t lt = (1u << lane) - 1u;
-  int gt_run = 0, eq_run = 0;  // counts in earlier chunks
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
-    int gt_before = gt_run, eq_before = eq_run, gt_tot = 0, eq_tot = 0;
-    for (int w2 = 0; w2 < kWarps; ++w2) {
-      const int a = wcnt[w2][j][0], b = wcnt[w2][j][1];
-      if (w2 < warp) {
-        gt_before += a;
-        eq_before += b;
-      }
-      gt_tot += a;
-      eq_tot += b;
-    }
+    const uint32_t pre = chunk_cnt[j * kWarps + warp];
     const int c = tid + j * kTopkThreads;
     const bool gt = (bg[j] >> lane) & 1u, eq = (be[j] >> lane) & 1u;
-    const int pg = gt_before + __popc(bg[j] & lt);
-    const int pe = eq_before + __popc(be[j] & lt);
+    const int pg = static_cast<int>(pre >> 16) + __popc(bg[j] & lt);
+    const int pe = static_cast<int>(pre & 0xffffu) + __popc(be[j] & lt);
     int slot = -1;
     if (gt) slot = pg + min(pe, need_eq);
     else if (eq && pe < need_eq) slot = pg + pe;
@@ -759,8 +843,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       out[slot] = token(c);
       if (colo) colo[slot] = c;
     }
-    gt_run += gt_tot;
-    eq_run += eq_tot;
   }
 }
 

@@ -180,6 +180,24 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Shared-memory descriptor of a 32-row x 16-byte matrix stored contiguously
+// (no swizzle; 8-row groups 128 bytes apart), the source of a 32x128b copy.
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1) << 46;         // descriptor version
+  return d;
+}
+
+// Copy a 32-row x 128-bit matrix from shared memory into 4 TMEM columns of
+// every lane quarter: lane 32q + i, column base + c receives word 4i + c.
+// Ordered with the tcgen05.mma this thread issues afterwards.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
