@@ -196,10 +196,11 @@ int score_grid(const smq_plan* p, int rows) {
 // Scratch of sparse_mqa_logits_topk_decode_noalloc: a status header, then
 // the fp32 logits. Some callers cannot hand the library a workspace: a
 // runtime whose device memory all belongs to its own pool and is not lent
-// out, or a plugin that may touch only the buffers it was handed. For them the scratch is part of the
-// loaded module, one copy on every device the library is loaded on. Only the
-// status word must start at zero (each call clears it); the score kernel
-// writes every logits column it covers before top-k reads it.
+// out, or a plugin that may touch only the buffers it was handed. For them
+// the scratch is part of the loaded module, one copy on every device the
+// library is loaded on. Only the status word must start at zero (each call
+// clears it); the score kernel writes every logits column it covers before
+// top-k reads it.
 static __device__ __align__(256) uint8_t smq_noalloc_scratch[kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -357,13 +358,22 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   CUtensorMap tm_q;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
   if (rc != SMQ_OK) return rc;
+  // up to 64 candidate blocks per row the score kernel expands the rows itself
+  const bool fused = !a.expansion_ready && plan->desc.candidate_topk_blocks <= smq::kMaxFusedBlocks;
   record(a.profile_events[0], s);
-  if (!a.expansion_ready) {
+  if (!a.expansion_ready && !fused) {
     rc = run_expand(plan, a.candidate_blocks, nullptr, a.row_ke, a.rows, a.sparse_indices, a.end, s);
     if (rc != SMQ_OK) return rc;
   }
   record(a.profile_events[1], s);
   smq::ScoreParams sp = score_params(plan, c);
+  sp.fused = fused ? 1 : 0;
+  sp.ncb = plan->desc.candidate_topk_blocks;
+  sp.cbs = plan->desc.candidate_block_size;
+  sp.candidate_blocks = a.candidate_blocks;
+  sp.row_ke = a.row_ke;
+  sp.sparse_indices_out = a.sparse_indices;
+  sp.end_out = a.end;
   sp.k_cache = a.k_cache;
   sp.num_pages = a.num_pages;
   sp.page_bytes = plan->page_bytes;

@@ -56,7 +56,7 @@ struct SubBlockSrc {
 
 // Byte offsets inside the score kernel's dynamic shared memory (base aligned to 1024).
 struct ScoreLayout {
-  uint32_t kv, q, sf, desc, w, w_stride, meta, bars, misc, scan, prefix, total;
+  uint32_t kv, q, sf, desc, w, w_stride, meta, bars, misc, scan, sched, prefix, rend, total;
   __host__ __device__ ScoreLayout(int n_mma, int heads, int rows) {
     uint32_t o = 0;
     kv = o;  // [stages][128 rows][128 B] padded FP4 keys, 128-byte swizzle
@@ -79,8 +79,12 @@ struct ScoreLayout {
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
     o += 64u;
+    sched = o;  // the scheduler's sorted candidate blocks of its current row
+    o += kMaxFusedBlocks * 4u;
     prefix = o;  // [rows + 1] exclusive prefix of tiles per row
     o += round_up((static_cast<uint32_t>(rows) + 1u) * 4u, 16);
+    rend = o;  // [rows] the end of each row this CTA expands, by local row index
+    o += round_up(static_cast<uint32_t>(rows) * 4u, 16);
     total = o;
   }
 };
@@ -227,7 +231,91 @@ __device__ __forceinline__ SubBlockSrc get_src(const SubBlockSrc* e) {
   return d;
 }
 
-template <bool kPaged, int kN>
+__device__ __forceinline__ void st_volatile_s32(int32_t* a, int32_t v) {
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(smem_addr(a)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_volatile_s32(const int32_t* a) {
+  int32_t v;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(a)) : "memory");
+  return v;
+}
+
+// Candidate expansion of row r by one warp, for at most 64 candidate blocks
+// (the same result as expand_kernel): a block is kept if it lies in [0, L)
+// and no earlier candidate has the same id; the kept blocks are sorted into
+// sorted[0 .. nkept). Returns the row's column count. When `owner` is set
+// the row's sparse_indices and end are written to global memory.
+__device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_t* sorted, bool owner, int lane) {
+  const int ncb = p.ncb;
+  const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * ncb;
+  const int c0 = lane < ncb ? cb[lane] : -1;
+  const int c1 = lane + 32 < ncb ? cb[lane + 32] : -1;
+  const uint32_t lt = (1u << lane) - 1u;
+  auto in_range = [&](int b) { return b >= 0 && static_cast<int64_t>(b) * p.cbs < L; };
+  // first occurrence: no lower lane (and for c1 no c0 at all) holds the same id.
+  // Every lane takes part in each warp vote, so the votes come first and the
+  // per-lane conditions after them.
+  const uint32_t same0 = __match_any_sync(kFullMask, c0);
+  const bool keep0 = lane < ncb && in_range(c0) && (same0 & lt) == 0;
+  bool keep1 = false;
+  if (ncb > 32) {
+    const uint32_t same1 = __match_any_sync(kFullMask, c1);
+    bool dup = (same1 & lt) != 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) dup |= __shfl_sync(kFullMask, c0, j) == c1;
+    keep1 = lane + 32 < ncb && in_range(c1) && !dup;
+  }
+  const int k0 = keep0 ? c0 : INT_MAX, k1 = keep1 ? c1 : INT_MAX;
+  int rank0 = 0, rank1 = 0;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) {
+    const int a = __shfl_sync(kFullMask, k0, j);
+    rank0 += a < k0;
+    rank1 += a < k1;
+  }
+  if (ncb > 32) {
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int b = __shfl_sync(kFullMask, k1, j);
+      rank0 += b < k0;
+      rank1 += b < k1;
+    }
+  }
+  const int nkept = __popc(__ballot_sync(kFullMask, keep0)) + __popc(__ballot_sync(kFullMask, keep1));
+  if (keep0) sorted[rank0] = c0;
+  if (keep1) sorted[rank1] = c1;
+  const int sbkv = p.sbkv, spb = p.cbs / p.sbkv;
+  int64_t cols = 0;
+  for (int u = 0; u < spb; ++u) {
+    if (keep0) {
+      const int64_t start = (static_cast<int64_t>(c0) * spb + u) * sbkv;
+      if (start < L) cols += L - start < sbkv ? L - start : sbkv;
+    }
+    if (keep1) {
+      const int64_t start = (static_cast<int64_t>(c1) * spb + u) * sbkv;
+      if (start < L) cols += L - start < sbkv ? L - start : sbkv;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) cols += __shfl_xor_sync(kFullMask, cols, o);
+  __syncwarp();
+  if (owner) {
+    int32_t* si = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
+    for (int slot = lane; slot < p.nsb; slot += 32) {
+      const int k = slot / spb;
+      int v = -1;
+      if (k < nkept) {
+        const int sub = sorted[k] * spb + slot % spb;
+        if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
+      }
+      si[slot] = v;
+    }
+    if (lane == 0) p.end_out[r] = static_cast<int32_t>(cols);
+  }
+  return static_cast<int>(cols);
+}
+
+template <bool kPaged, int kN, bool kFused>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ uint8_t score_smem_raw[];
@@ -287,15 +375,23 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // previous kernel; everything below reads what earlier kernels wrote
   griddep_launch_dependents();
   griddep_wait();
+  // tiles of row r: from its end, or (rows expanded here) the bound ceil(min(row_ke, S) / 128)
   const int per = (R + kScoreThreads - 1) / kScoreThreads;
   const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
   auto tiles_of = [&](int r) {
-    int e = p.end[r];
+    int e = kFused ? p.row_ke[r] : p.end[r];
     e = e < 0 ? 0 : (e > S ? S : e);
     return (e + kTileM - 1) / kTileM;
   };
   int mine = 0;
-  for (int r = r0; r < r1; ++r) mine += tiles_of(r);
+  for (int r = r0; r < r1; ++r) {
+    const int nt = tiles_of(r);
+    mine += nt;
+    if (kFused && nt == 0 && blockIdx.x == 0) {  // no column at all: CTA 0 writes the empty expansion
+      for (int slot = 0; slot < p.nsb; ++slot) p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = -1;
+      p.end_out[r] = 0;
+    }
+  }
   int incl = mine;
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(kFullMask, incl, o);
@@ -347,7 +443,79 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int sbkv = p.sbkv;
   const int H = p.heads;
 
-  if (warp == 0) {
+  if (warp == 0 && kFused) {
+    // ======================= scheduler (rows expanded here) =======================
+    // Row by row: expand the row (sorted candidate blocks and end), then
+    // resolve its tiles in this CTA in batches of 32 / spt, each lane one
+    // sub-block to its page. Tiles past the row's end are published empty.
+    const int tiles_per_batch = 32 / spt;
+    const int spb = p.cbs / sbkv;
+    int32_t* sorted = reinterpret_cast<int32_t*>(smem + lay.sched);
+    int32_t* rend = reinterpret_cast<int32_t*>(smem + lay.rend);
+    const int r_first = find_row(prefix, R, t_begin);
+    int it = 0;
+    bool ok = true;
+    for (int r = r_first; ok && r < R && prefix[r] < t_end; ++r) {
+      const int64_t row0 = prefix[r];
+      const int64_t rz = prefix[r + 1];
+      if (rz == row0) continue;  // no tiles (written by CTA 0)
+      const int brow = p.row_indices ? p.row_indices[r] : r;
+      const int ke = p.row_ke[r];
+      int e = expand_row_in_warp(p, r, ke > 0 ? ke : 0, sorted, row0 >= t_begin, lane);
+      e = e < 0 ? 0 : (e > S ? S : e);
+      // read by the epilogue once it sees this row's first accumulator
+      if (lane == 0) st_volatile_s32(rend + (r - r_first), e);
+      __syncwarp();
+      const int64_t ta = row0 > t_begin ? row0 : t_begin;
+      const int64_t tz = rz < t_end ? rz : t_end;
+      for (int64_t tb = ta; tb < tz && ok; tb += tiles_per_batch) {
+        const int64_t t = tb + lane / spt;
+        const int sub = lane % spt;
+        const int col_sub = static_cast<int>(t - row0) * spt + sub;
+        int ntok = 0;
+        const uint8_t* vsrc = nullptr;
+        const uint8_t* ssrc = nullptr;
+        if (t < tz && col_sub * sbkv < e) {  // columns below end are valid sub-blocks
+          const int sb = sorted[col_sub / spb] * spb + col_sub % spb;
+          const int64_t tpos = static_cast<int64_t>(sb) * sbkv;
+          const int64_t slot = tpos / p.page_size;
+          bool valid = false;
+          if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride) {
+            const int pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
+            if (pg >= 0 && pg < p.num_pages) {
+              const int64_t tok = tpos % p.page_size;
+              const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
+              vsrc = base + tok * (kHeadDim / 2);
+              ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+              ntok = sbkv;
+              valid = true;
+            }
+          }
+          if (!valid) set_status(p.status, kStatusBounds);
+        }
+        for (int k = 0; k < tiles_per_batch; ++k) {
+          if (tb + k >= tz) break;
+          const int base = k * spt;
+          const int dslot = it % kDescRing;
+          bool e_ok = true;
+          if (lane == 0)
+            e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane >= base && lane < base + spt) put_src(&desc[dslot * 8 + (lane - base)], vsrc, ssrc, ntok);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_desc_full(dslot));
+          ++it;
+        }
+      }
+      __syncwarp();  // `sorted` is rewritten for the next row
+    }
+    if (!ok) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ======================= scheduler =======================
     // Resolves each tile's sub-blocks to source addresses (row, sparse id,
     // block-table page, bounds), publishes them per stage, and loads the
@@ -444,9 +612,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int qb = quse & 1;
         ok = mbar_wait(bar_q_empty(qb), ((quse >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
-        int e = p.end[r];
         meta[qb].row = r;
-        meta[qb].end = e < 0 ? 0 : (e > S ? S : e);
+        if constexpr (!kFused) {  // expanded rows' ends come from the scheduler
+          const int e = p.end[r];
+          meta[qb].end = e < 0 ? 0 : (e > S ? S : e);
+        }
         meta[qb].q_scale = p.q_scale[r];
         const uint32_t q_dst = smem_addr(smem + lay.q + qb * kN * kRowBytes);
         const uint32_t w_dst = smem_addr(smem + lay.w + qb * lay.w_stride);
@@ -524,7 +694,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int m = 32 * q4 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     int r = find_row(prefix, R, t_begin);
+    const int r_first = r;
     int cur = -1, qb = 0, row = 0, e = 0;
+    bool need_end = false;
     uint32_t quse = 0;
     float qs = 0.f;
     float w[kN];
@@ -533,13 +705,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int64_t t = t_begin + ie;
       while (prefix[r + 1] <= t) ++r;
       if (r != cur) {
+        need_end = kFused;
         cur = r;
         qb = quse & 1;
         ok = warp_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, kWaitLimitNs);
         ++quse;
         if (!ok) break;
         row = meta[qb].row;
-        e = meta[qb].end;
+        if constexpr (!kFused) e = meta[qb].end;
         qs = meta[qb].q_scale;
         const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w + qb * lay.w_stride);
 #pragma unroll
@@ -549,6 +722,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int a = ie % NA;
       ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
       if (!ok) break;
+      if (need_end) {  // written by the scheduler before it published this row's first tile
+        e = ld_volatile_s32(reinterpret_cast<const int32_t*>(smem + lay.rend) + (r - r_first));
+        need_end = false;
+      }
       // the MMAs of this tile have finished: its key stage and scale columns are free
       if (warp == 2 && lane == 0) mbar_arrive(bar_empty(ie % NS));
       tc_fence_after();
@@ -895,10 +1072,12 @@ cudaError_t prepare_kernels(int n_mma) {
   cudaError_t err;
   // one shared-memory carveout for every kernel of a step, so that consecutive
   // kernels never wait for the SM to re-split L1 and shared memory
-  const void* all[] = {reinterpret_cast<const void*>(&score_kernel<true, 64>),
-                       reinterpret_cast<const void*>(&score_kernel<false, 64>),
-                       reinterpret_cast<const void*>(&score_kernel<true, 128>),
-                       reinterpret_cast<const void*>(&score_kernel<false, 128>),
+  const void* all[] = {reinterpret_cast<const void*>(&score_kernel<true, 64, true>),
+                       reinterpret_cast<const void*>(&score_kernel<true, 64, false>),
+                       reinterpret_cast<const void*>(&score_kernel<false, 64, false>),
+                       reinterpret_cast<const void*>(&score_kernel<true, 128, true>),
+                       reinterpret_cast<const void*>(&score_kernel<true, 128, false>),
+                       reinterpret_cast<const void*>(&score_kernel<false, 128, false>),
                        reinterpret_cast<const void*>(&topk_kernel<8>),
                        reinterpret_cast<const void*>(&topk_kernel<16>),
                        reinterpret_cast<const void*>(&topk_kernel<32>),
@@ -908,14 +1087,16 @@ cudaError_t prepare_kernels(int n_mma) {
     err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
   }
-  if (n_mma == 64) {
-    err = cudaFuncSetAttribute(score_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  const void* score[] = {reinterpret_cast<const void*>(&score_kernel<true, 64, true>),
+                         reinterpret_cast<const void*>(&score_kernel<true, 64, false>),
+                         reinterpret_cast<const void*>(&score_kernel<false, 64, false>),
+                         reinterpret_cast<const void*>(&score_kernel<true, 128, true>),
+                         reinterpret_cast<const void*>(&score_kernel<true, 128, false>),
+                         reinterpret_cast<const void*>(&score_kernel<false, 128, false>)};
+  for (int i = 0; i < 6; ++i) {
+    if ((i < 3) != (n_mma == 64)) continue;
+    err = cudaFuncSetAttribute(score[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(score_kernel<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  } else {
-    err = cudaFuncSetAttribute(score_kernel<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(score_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   }
   if (err != cudaSuccess) return err;
 
@@ -966,11 +1147,15 @@ cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
 
 cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
                          cudaStream_t stream) {
-  if (paged)
-    return p.n_mma == 64 ? launch_pdl2(score_kernel<true, 64>, grid, kScoreThreads, smem, stream, p, tm_q)
-                         : launch_pdl2(score_kernel<true, 128>, grid, kScoreThreads, smem, stream, p, tm_q);
-  return p.n_mma == 64 ? launch_pdl2(score_kernel<false, 64>, grid, kScoreThreads, smem, stream, p, tm_q)
-                       : launch_pdl2(score_kernel<false, 128>, grid, kScoreThreads, smem, stream, p, tm_q);
+  const bool stat = paged && p.fused;
+  if (p.n_mma == 64) {
+    if (stat) return launch_pdl2(score_kernel<true, 64, true>, grid, kScoreThreads, smem, stream, p, tm_q);
+    if (paged) return launch_pdl2(score_kernel<true, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q);
+    return launch_pdl2(score_kernel<false, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q);
+  }
+  if (stat) return launch_pdl2(score_kernel<true, 128, true>, grid, kScoreThreads, smem, stream, p, tm_q);
+  if (paged) return launch_pdl2(score_kernel<true, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q);
+  return launch_pdl2(score_kernel<false, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q);
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {

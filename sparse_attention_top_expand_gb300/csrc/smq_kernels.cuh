@@ -23,6 +23,7 @@ constexpr int kScoreStages = 8;     // key tiles resident in shared memory
 constexpr int kLoadAhead = 6;       // tiles each loader thread keeps in flight (< kScoreStages)
 constexpr int kMaxAccBuffers = 4;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
+constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
 
 // TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 3 x 128 fp32 columns.
 __host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 3; }
@@ -66,6 +67,16 @@ struct ScoreParams {
   const uint8_t* k_values;
   const uint8_t* k_scales;
   int64_t total_len;
+  // in-kernel candidate expansion (paged decode, at most kMaxFusedBlocks candidate blocks):
+  // tiles are spread over rows by an upper bound from row_ke alone, ceil(min(row_ke, num_cols) / kTileM),
+  // and each CTA expands its own rows, writing sparse_indices_out / end_out
+  int32_t fused;
+  int32_t ncb;            // candidate blocks per row
+  int32_t cbs;            // candidate block size
+  const int32_t* candidate_blocks;
+  const int32_t* row_ke;
+  int32_t* sparse_indices_out;
+  int32_t* end_out;
   // outputs
   float* logits;     // [rows][num_cols]
   int32_t* status;   // workspace status word
@@ -119,7 +130,7 @@ size_t score_smem_bytes(int n_mma, int heads, int rows);
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
 cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
-                         cudaStream_t stream);
+                         cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
