@@ -822,18 +822,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           const SubBlockSrc* dring = desc + dslot * 8;
+          // every entry first (the reads are ordered, so batching them keeps
+          // each global load from waiting on its own shared read)
+          SubBlockSrc d[4];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) d[k4] = get_src(dring + vu[k4]);
+          const SubBlockSrc ds = get_src(dring + su);
           uint32_t hv = 0;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const SubBlockSrc d = get_src(dring + vu[k4]);
-            if (d.values != nullptr && vtk[k4] < d.positions) {
-              v[k][k4] = ldg_stream_v4(d.values + static_cast<int64_t>(vtk[k4]) * (kHeadDim / 2) + 16 * vch);
+            if (d[k4].values != nullptr && vtk[k4] < d[k4].positions) {
+              v[k][k4] = ldg_stream_v4(d[k4].values + static_cast<int64_t>(vtk[k4]) * (kHeadDim / 2) + 16 * vch);
               hv |= 1u << k4;
             }
           }
           have[k] = hv;
           sw[k] = 0x7F7F7F7Fu;
-          const SubBlockSrc ds = get_src(dring + su);
           if (ds.values != nullptr && stk < ds.positions)
             sw[k] = ldg_stream_u32(ds.scales + static_cast<int64_t>(stk) * kScaleWordBytes);
           __syncwarp();  // every lane has read the entry before it is handed back
@@ -860,13 +864,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
 // Thread t holds the keys of columns t, t + 512, t + 1024, ... in registers.
-// Up to three digit passes (11, 11, 10 bits, most significant first) build a
-// shared-memory histogram of the keys that still match the selected prefix;
-// a descending block scan over the bins finds the bin that holds the k-th
-// largest key. The passes stop early once every key of the selected bin is
-// taken. Then every key above the selected prefix, and the first `need` keys
-// inside it in column order, are written by one ordered compaction: a single
-// scan over the per-32-column counts gives each warp its output offsets.
+// Up to four digit passes of 8 bits (most significant first) count the keys
+// that still match the selected prefix; the bin holding the k-th largest key
+// is found by a descending scan over the 256 bins. The histogram keeps one
+// copy per lane (bin b, copy l at word 32 b + l, bank l), so the atomic
+// increments of a warp never touch the same word or bank even when most keys
+// fall into a few bins, as logits do. The passes stop once every key of the
+// selected bin is taken. Then every key above the selected prefix, and the
+// first `need` keys inside it in column order, are written by one ordered
+// compaction: a single scan over the per-32-column counts gives each warp its
+// output offsets.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -875,13 +882,14 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 template <int kJ>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkParams p) {
   constexpr int kWarps = kTopkThreads / 32;
-  constexpr int kBins = 2048;
+  constexpr int kBins = 256;
   constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
   extern __shared__ int32_t sidx[];     // [nsb] sparse sub-block ids of the row
-  __shared__ int hist[2][kBins];
+  __shared__ __align__(16) uint32_t hist[kBins * 32];
+  __shared__ int bsum[kBins];
   __shared__ int wsum[kWarps];
   __shared__ uint32_t chunk_cnt[kChunks];  // (above << 16) | inside, then their exclusive prefix
-  __shared__ int sel_bin[3], sel_above[3], sel_cnt[3];
+  __shared__ int sel_bin[4], sel_above[4], sel_cnt[4];
   griddep_launch_dependents();
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -900,7 +908,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   int e = p.end[r];
   e = e < 0 ? 0 : (e > S ? S : e);
   for (int i = tid; i < p.nsb; i += kTopkThreads) sidx[i] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + i];
-  for (int i = tid; i < kBins; i += kTopkThreads) hist[0][i] = 0;
+  uint4* hist4 = reinterpret_cast<uint4*>(hist);
+  for (int i = tid; i < kBins * 8; i += kTopkThreads) hist4[i] = make_uint4(0, 0, 0, 0);
   if (p.logits_fill)
     for (int c = e + tid; c < S; c += kTopkThreads) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
   int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
@@ -920,53 +929,52 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   uint32_t prefix = 0;  // selected high bits so far
   int need = k;         // keys still to take among those matching the prefix
   int done_bits = 0;
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int wbits = widths[pass];
-    const int shift = 32 - done_bits - wbits;
-    const int nb = 1 << wbits;
-    int* h = hist[pass & 1];
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - done_bits;
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int c = tid + j * kTopkThreads;
       const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
-      if (match) atomicAdd(&h[(key[j] >> shift) & (nb - 1)], 1);
+      if (match) atomicAdd(&hist[((key[j] >> shift) & (kBins - 1)) * 32 + lane], 1u);
     }
     __syncthreads();
-    // the other buffer was last read before the previous pass's second barrier
-    for (int i = tid; i < kBins; i += kTopkThreads) hist[(pass + 1) & 1][i] = 0;
-    // descending scan: thread t owns bins nb-1-4t .. nb-4-4t (4 bins; fewer threads when nb = 1024)
-    int cnt[4];
-    int local = 0;
+    {  // bin totals: two threads per bin, 16 copies each, read in a rotated order (no bank conflicts)
+      const int b = tid >> 1, h = tid & 1;
+      int sum = 0;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int bin = nb - 1 - 4 * tid - b;
-      cnt[b] = bin >= 0 ? h[bin] : 0;
-      local += cnt[b];
+      for (int i = 0; i < 16; ++i) sum += static_cast<int>(hist[b * 32 + ((h * 16 + i + b) & 31)]);
+      sum += __shfl_xor_sync(kFullMask, sum, 1);
+      if (h == 0) bsum[b] = sum;
     }
-    int incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(kFullMask, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    int cum = incl - local;
-#pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) cum += w2 < warp ? wsum[w2] : 0;  // independent loads
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      if (cnt[b] > 0 && cum < need && need <= cum + cnt[b]) {
-        sel_bin[pass] = nb - 1 - 4 * tid - b;
-        sel_above[pass] = cum;
-        sel_cnt[pass] = cnt[b];
+    // descending scan: thread t < 256 owns bin 255 - t
+    int cnt = 0, incl = 0;
+    if (tid < kBins) {
+      cnt = bsum[kBins - 1 - tid];
+      incl = cnt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += v;
       }
-      cum += cnt[b];
+      if (lane == 31) wsum[warp] = incl;
+    }
+    // every histogram read of this pass is done: clear it for the next one
+    for (int i = tid; i < kBins * 8; i += kTopkThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (tid < kBins) {
+      int cum = incl - cnt;
+#pragma unroll
+      for (int w2 = 0; w2 < kBins / 32; ++w2) cum += w2 < warp ? wsum[w2] : 0;  // independent loads
+      if (cnt > 0 && cum < need && need <= cum + cnt) {
+        sel_bin[pass] = kBins - 1 - tid;
+        sel_above[pass] = cum;
+        sel_cnt[pass] = cnt;
+      }
     }
     __syncthreads();
-    prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin[pass]);
+    prefix = (prefix << 8) | static_cast<uint32_t>(sel_bin[pass]);
     need -= sel_above[pass];
-    done_bits += wbits;
+    done_bits += 8;
     if (need == sel_cnt[pass]) break;  // the whole bin is taken
   }
   // selected: keys whose top done_bits bits are above the prefix, and the
