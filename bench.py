@@ -300,8 +300,10 @@ def run_ours(args, rank, world, dist):
                                               d.row_indices, d.row_ke, d.candidate_blocks, d.topk_out,
                                               d.sparse_indices, d.end, d.workspace, profile_events=events)
 
-    launches_per_step = {"decode_batch": 3, "long_context_decode": 3, "prefill_chunk": 4,
-                         "shared_schedule": 1 + 2 * len(layers)}[args.workload]
+    # decode rows with at most 64 candidate blocks are expanded inside the score kernel
+    decode_launches = 2 if base.geom.candidate_topk_blocks <= 64 else 3
+    launches_per_step = {"decode_batch": decode_launches, "long_context_decode": decode_launches,
+                         "prefill_chunk": 4, "shared_schedule": 1 + 2 * len(layers)}[args.workload]
 
     for i in range(args.warmup):
         step(i)
