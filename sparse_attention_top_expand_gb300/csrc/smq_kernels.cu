@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // ---- prologue: barriers, per-row tile counts and their prefix ---------
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full(s), kLoaderThreads);
+      mbar_init(bar_full(s), kLoaderThreads / 32);  // one arrival per loader warp
       mbar_init(bar_empty(s), 1);
     }
     for (int d = 0; d < kDescRing; ++d) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     for (int a = 0; a < NA; ++a) {
       mbar_init(bar_acc_full(a), 1);
-      mbar_init(bar_acc_empty(a), kEpilogueThreads);
+      mbar_init(bar_acc_empty(a), kEpilogueThreads / 32);  // one arrival per epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_q_full(b), 1);
@@ -658,13 +658,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           cur = r;
           qb = quse & 1;
           ++quse;
+          // both threads wait for every row's query, so that neither can skip a
+          // phase of a buffer and later match its parity too early
+          ok = mbar_wait(bar_q_full(qb), ((quse - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
         }
         const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
         if ((it & 1) == par) {
           const int s = it % NS;
           const int a = it % NA;
-          ok = mbar_wait(bar_q_full(qb), ((quse - 1) >> 1) & 1, abort_flag, kWaitLimitNs) &&
-               mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
+          ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
                mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
@@ -739,9 +742,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tmem_ld16(tacc + c, v0);
         tmem_ld16(tacc + c + 16, v1);
         tmem_wait_ld();
-        if (c + 32 >= kN) {  // every column read: hand the accumulator back
+        if (c + 32 >= kN) {  // every column read: hand the accumulator back, one arrival per warp
           tc_fence_before();
-          mbar_arrive(bar_acc_empty(a));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acc_empty(a));
         }
 #pragma unroll
         for (int h = 0; h < 16; ++h)
@@ -814,8 +818,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // scale word of key row m: word 4 (m % 32) + m / 32 of the stage's block,
           // which the copy to TMEM places at lane m, column base + m / 32
           sts_u32(sf_base + s * 512 + 16 * lane + 4 * q4, sw[k]);
-          fence_proxy_async_smem();  // make the stores visible to the tensor core's reads
-          mbar_arrive(bar_full(s));
+          fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
+          __syncwarp();  // one arrival per warp
+          if (lane == 0) mbar_arrive(bar_full(s));
         }
         if (i < n) {
           const int dslot = i % kDescRing;

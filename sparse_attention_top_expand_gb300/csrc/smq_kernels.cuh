@@ -25,8 +25,11 @@ constexpr int kMaxAccBuffers = 4;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
 
-// TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 3 x 128 fp32 columns.
-__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 3; }
+// TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 2 x 128 fp32 columns.
+// The count is even: tiles it and it - NA then have the same parity, so both go
+// to the same MMA thread, whose own earlier wait keeps its parity waits on that
+// accumulator from running two phases ahead.
+__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 2; }
 
 // TMEM columns per CTA: accumulators, then 4 scale columns per stage, then 4 for the query scales.
 __host__ __device__ constexpr int score_tmem_columns(int n_mma) {
