@@ -59,14 +59,14 @@ struct ScoreLayout {
   uint32_t kv, q, sf, desc, w, w_stride, meta, bars, misc, scan, sched, prefix, rend, total;
   __host__ __device__ ScoreLayout(int n_mma, int heads, int rows) {
     uint32_t o = 0;
-    kv = o;  // [stages][128 rows][128 B] padded FP4 keys, 128-byte swizzle
+    kv = o;  // [stages][256 rows][128 B] padded FP4 keys, 128-byte swizzle (two 128-row MMA halves)
     o += static_cast<uint32_t>(kScoreStages) * kTileM * kRowBytes;
     q = o;  // [2][n_mma rows][128 B] E4M3 queries, 128-byte swizzle
     o += 2u * static_cast<uint32_t>(n_mma) * kRowBytes;
-    sf = o;  // [stages][32 rows][16 B] key scale words, copied to TMEM by the MMA thread; then one block of 2^0
-    o += static_cast<uint32_t>(kScoreStages + 1) * 512u;
+    sf = o;  // [stages][halves][32 rows][16 B] key scale words, copied to TMEM by the MMA thread; then one block of 2^0
+    o += static_cast<uint32_t>(kScoreStages * kHalves + 1) * 512u;
     desc = o;  // [ring][8 sub-blocks] source addresses published by the scheduler warp
-    o += static_cast<uint32_t>(kDescRing) * 8u * sizeof(SubBlockSrc);
+    o += static_cast<uint32_t>(kDescRing) * kMaxSubsPerTile * sizeof(SubBlockSrc);
     w_stride = round_up(static_cast<uint32_t>(heads) * 2u, 16);
     w = o;  // [2][heads] bf16 weights
     o += 2u * w_stride;
@@ -419,11 +419,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_sfa = tmem + NA * kN;
-  const uint32_t tm_sfb = tm_sfa + 4 * NS;
+  const uint32_t tm_sfa = tmem + NA * kHalves * kN;
+  const uint32_t tm_sfb = tm_sfa + 4 * kHalves * NS;
   // B (query) scales are all 2^0: one 512-byte block of 0x7F copied to the
   // SF-B columns by the first MMA thread, complete before any MMA is issued
-  uint32_t* sf_one = reinterpret_cast<uint32_t*>(smem + lay.sf + kScoreStages * 512);
+  uint32_t* sf_one = reinterpret_cast<uint32_t*>(smem + lay.sf + kScoreStages * kHalves * 512);
   if (tid < 128) sf_one[tid] = 0x7F7F7F7Fu;
   fence_proxy_async_smem();
   __syncthreads();
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
           ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          if (lane >= base && lane < base + spt) put_src(&desc[dslot * 8 + (lane - base)], vsrc, ssrc, ntok);
+          if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, ntok);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_desc_full(dslot));
           ++it;
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the lanes that resolved this tile's sub-blocks publish them
-        if (lane >= base && lane < base + spt) put_src(&desc[dslot * 8 + (lane - base)], vsrc, ssrc, ntok);
+        if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, ntok);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_desc_full(dslot));
         ++it;
@@ -646,7 +646,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
       uint32_t idesc[4];
-      for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kTileM, kN, g, g);
+      for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kMmaM, kN, g, g);
       int r = find_row(prefix, R, t_begin);
       int cur = -1, qb = 0;
       uint32_t quse = 0;
@@ -664,19 +664,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (!ok) break;
         }
         const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
-        if ((it & 1) == par) {
+        // an even accumulator count: alternate stages; otherwise the first thread issues all
+        if ((NA % 2 == 0) ? ((it & 1) == par) : (par == 0)) {
           const int s = it % NS;
           const int a = it % NA;
           ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
                mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
-          // the stage's key scales: shared memory -> TMEM, in order before the MMAs below
-          tmem_cp_32x128b_x4(tm_sfa + 4 * s, rows16_desc(smem_addr(smem + lay.sf + s * 512)));
-          const uint64_t adesc = sw128_desc(smem_addr(smem + lay.kv + s * (kTileM * kRowBytes)));
+          const uint32_t stage_addr = smem_addr(smem + lay.kv + s * (kTileM * kRowBytes));
           const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q + qb * kN * kRowBytes));
-          for (int g = 0; g < 4; ++g)  // K = 32 per MMA; advance 32 bytes along the swizzled rows
-            mma_mxf8f6f4(tmem + a * kN, adesc + 2 * g, bdesc + 2 * g, idesc[g], tm_sfa + 4 * s, tm_sfb, g > 0);
+          for (int h = 0; h < kHalves; ++h) {
+            // this half's key scales: shared memory -> TMEM, in order before its MMAs
+            const uint32_t sfa = tm_sfa + 4 * (s * kHalves + h);
+            tmem_cp_32x128b_x4(sfa, rows16_desc(smem_addr(smem + lay.sf + (s * kHalves + h) * 512)));
+            const uint64_t adesc = sw128_desc(stage_addr + h * (kMmaM * kRowBytes));
+            for (int g = 0; g < 4; ++g)  // K = 32 per MMA; advance 32 bytes along the swizzled rows
+              mma_mxf8f6f4(tmem + (a * kHalves + h) * kN, adesc + 2 * g, bdesc + 2 * g, idesc[g], sfa, tm_sfb,
+                           g > 0);
+          }
           mma_commit(bar_acc_full(a));
         }
         if (last_of_row) mma_commit(bar_q_empty(qb));
@@ -732,31 +738,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // the MMAs of this tile have finished: its key stage and scale columns are free
       if (warp == 2 && lane == 0) mbar_arrive(bar_empty(ie % NS));
       tc_fence_after();
-      // four independent partial sums keep the FMA pipe busy instead of one
-      // 64-deep dependent chain
-      float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t tacc = tmem + a * kN + lane_base;
 #pragma unroll
-      for (int c = 0; c < kN; c += 32) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(tacc + c, v0);
-        tmem_ld16(tacc + c + 16, v1);
-        tmem_wait_ld();
-        if (c + 32 >= kN) {  // every column read: hand the accumulator back, one arrival per warp
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_acc_empty(a));
+      for (int h = 0; h < kHalves; ++h) {
+        // four independent partial sums keep the FMA pipe busy instead of one
+        // 64-deep dependent chain
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t tacc = tmem + (a * kHalves + h) * kN + lane_base;
+#pragma unroll
+        for (int c = 0; c < kN; c += 32) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tacc + c, v0);
+          tmem_ld16(tacc + c + 16, v1);
+          tmem_wait_ld();
+          if (h == kHalves - 1 && c + 32 >= kN) {  // every column read: hand the accumulator back, one arrival per warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty(a));
+          }
+#pragma unroll
+          for (int hh = 0; hh < 16; ++hh)
+            acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+#pragma unroll
+          for (int hh = 0; hh < 16; ++hh)
+            acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
         }
-#pragma unroll
-        for (int h = 0; h < 16; ++h)
-          acc4[h & 3] = fmaf(w[c + h], fmaxf(__uint_as_float(v0[h]), 0.f), acc4[h & 3]);
-#pragma unroll
-        for (int h = 0; h < 16; ++h)
-          acc4[h & 3] = fmaf(w[c + 16 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc4[h & 3]);
+        const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        const int col = static_cast<int>(t - prefix[r]) * kTileM + h * kMmaM + m;
+        if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
       }
-      const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-      const int col = static_cast<int>(t - prefix[r]) * kTileM + m;
-      if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
       if (last_of_row) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty(qb));
@@ -769,28 +778,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   } else if (warp >= 6 && warp < 10) {
     // ======================= loaders (warps 6..9) =======================
     // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
-    // t / 4 + 32 k (k = 0..3), so that each warp load reads 512 contiguous
-    // bytes (8 rows of one sub-block). Scale words: thread t owns key row t.
-    // Both are loaded kLoadAhead tiles before they are needed. The values are
-    // stored into the 16-byte containers the MMA reads (8 data bytes per 16
-    // elements, 128-byte swizzle); the scale word goes to TMEM lane t, column
-    // base + t/32.
+    // t / 4 + 32 k (k = 0..7), so that each warp load reads 512 contiguous
+    // bytes (8 rows of one sub-block). Scale words: thread t owns key rows t
+    // and t + 128. Both are loaded kLoadAhead stages before they are needed.
+    // The values are stored into the 16-byte containers the MMA reads (8 data
+    // bytes per 16 elements, 128-byte swizzle); the scale words go to the
+    // stage half's scale block.
+    constexpr int kChunks = kTileM / 32;
     const int q4 = warp & 3;
     const int m = 32 * q4 + lane;
     const uint32_t sf_base = smem_addr(smem + lay.sf);
     const int vch = m & 3;
-    int vu[4], vtk[4];
+    int vu[kChunks], vtk[kChunks];
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-      const int pos = (m >> 2) + 32 * k4;
-      vu[k4] = pos / sbkv;
-      vtk[k4] = pos % sbkv;
+    for (int k8 = 0; k8 < kChunks; ++k8) {
+      const int pos = (m >> 2) + 32 * k8;
+      vu[k8] = pos / sbkv;
+      vtk[k8] = pos % sbkv;
     }
-    const int su = m / sbkv, stk = m % sbkv;
+    int su[kHalves], stk[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      su[h] = (m + h * kMmaM) / sbkv;
+      stk[h] = (m + h * kMmaM) % sbkv;
+    }
     const uint32_t kv_base = smem_addr(smem + lay.kv);
-    uint4 v[kLoadAhead][4];
-    uint32_t sw[kLoadAhead];
-    uint32_t have[kLoadAhead];  // bit k4: value chunk k4 was loaded
+    uint4 v[kLoadAhead][kChunks];
+    uint32_t sw[kLoadAhead][kHalves];
+    uint32_t have[kLoadAhead];  // bit k8: value chunk k8 was loaded
 #pragma unroll
     for (int k = 0; k < kLoadAhead; ++k) have[k] = 0;
     bool ok = true;
@@ -798,26 +813,27 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
       for (int k = 0; k < kLoadAhead; ++k) {
         const int i = i0 + k;
-        const int j = i - kLoadAhead;  // the tile whose data sits in slot k
+        const int j = i - kLoadAhead;  // the stage whose data sits in slot k
         if (j >= 0 && j < n) {
           const int s = j % NS;
-          // the stage is free once the MMAs of tile j - NS have finished
+          // the stage is free once the MMAs of stage j - NS have finished
           ok = warp_wait(bar_empty(s), ((j / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            if (have[k] & (1u << k4)) {
-              const int pos = (m >> 2) + 32 * k4;
+          for (int k8 = 0; k8 < kChunks; ++k8) {
+            if (have[k] & (1u << k8)) {
+              const int pos = (m >> 2) + 32 * k8;
               const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
               const uint32_t swz = static_cast<uint32_t>(pos & 7);
-              sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k4].x, v[k][k4].y);
-              sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k4].z, v[k][k4].w);
+              sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k8].x, v[k][k8].y);
+              sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k8].z, v[k][k8].w);
             }
           }
-          // scale word of key row m: word 4 (m % 32) + m / 32 of the stage's block,
-          // which the copy to TMEM places at lane m, column base + m / 32
-          sts_u32(sf_base + s * 512 + 16 * lane + 4 * q4, sw[k]);
+          // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
+          // half's block, which the copy to TMEM places at lane m, column base + m / 32
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, sw[k][h]);
           fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
           __syncwarp();  // one arrival per warp
           if (lane == 0) mbar_arrive(bar_full(s));
@@ -826,26 +842,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int dslot = i % kDescRing;
           ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
-          const SubBlockSrc* dring = desc + dslot * 8;
-          // every entry first (the reads are ordered, so batching them keeps
-          // each global load from waiting on its own shared read)
-          SubBlockSrc d[4];
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) d[k4] = get_src(dring + vu[k4]);
-          const SubBlockSrc ds = get_src(dring + su);
+          const SubBlockSrc* dring = desc + dslot * kMaxSubsPerTile;
           uint32_t hv = 0;
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            if (d[k4].values != nullptr && vtk[k4] < d[k4].positions) {
-              v[k][k4] = ldg_stream_v4(d[k4].values + static_cast<int64_t>(vtk[k4]) * (kHeadDim / 2) + 16 * vch);
-              hv |= 1u << k4;
+          for (int k8 = 0; k8 < kChunks; ++k8) {
+            const SubBlockSrc d = get_src(dring + vu[k8]);
+            if (d.values != nullptr && vtk[k8] < d.positions) {
+              v[k][k8] = ldg_stream_v4(d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch);
+              hv |= 1u << k8;
             }
           }
           have[k] = hv;
-          sw[k] = 0x7F7F7F7Fu;
-          if (ds.values != nullptr && stk < ds.positions)
-            sw[k] = ldg_stream_u32(ds.scales + static_cast<int64_t>(stk) * kScaleWordBytes);
-          __syncwarp();  // every lane has read the entry before it is handed back
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h) {
+            const SubBlockSrc ds = get_src(dring + su[h]);
+            sw[k][h] = 0x7F7F7F7Fu;
+            if (ds.values != nullptr && stk[h] < ds.positions)
+              sw[k][h] = ldg_stream_u32(ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes);
+          }
+          __syncwarp();  // every lane has read the entries before they are handed back
           if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
         }
       }

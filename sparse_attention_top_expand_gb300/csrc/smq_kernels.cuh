@@ -11,7 +11,10 @@
 namespace smq {
 
 constexpr int kHeadDim = 128;       // D
-constexpr int kTileM = 128;         // key positions per MMA tile (the M of the MMA)
+constexpr int kMmaM = 128;          // key positions per MMA (its M)
+constexpr int kTileM = 256;         // key positions per pipeline stage: two MMA halves
+constexpr int kHalves = kTileM / kMmaM;
+constexpr int kMaxSubsPerTile = kTileM / 16;  // sparse sub-blocks per stage (they hold at least 16 positions)
 constexpr int kRowBytes = 128;      // smem bytes per K row (padded FP4) and per Q row (E4M3)
 constexpr int kScaleWordBytes = 4;  // D/32 UE8M0 bytes per key position
 constexpr int kScoreThreads = 384;  // scheduler, 2 MMA, 4 epilogue, 4 loader and 1 query-loader warps
@@ -19,21 +22,23 @@ constexpr int kQueryWarp = 10;
 constexpr int kMmaWarp1 = 11;       // second MMA issuer (odd tiles); warp 1 issues the even tiles
 constexpr int kEpilogueThreads = 128;
 constexpr int kLoaderThreads = 128;
-constexpr int kScoreStages = 8;     // key tiles resident in shared memory
-constexpr int kLoadAhead = 6;       // tiles each loader thread keeps in flight (< kScoreStages)
-constexpr int kMaxAccBuffers = 4;
+constexpr int kScoreStages = 4;     // key stages resident in shared memory (32 KB each)
+constexpr int kLoadAhead = 3;       // stages each loader thread keeps in flight in registers
+constexpr int kMaxAccBuffers = 2;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
 
-// TMEM accumulators in flight between the MMA and the epilogue: 4 x 64 or 2 x 128 fp32 columns.
-// The count is even: tiles it and it - NA then have the same parity, so both go
-// to the same MMA thread, whose own earlier wait keeps its parity waits on that
-// accumulator from running two phases ahead.
-__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 4 : 2; }
+// TMEM accumulators in flight between the MMA and the epilogue, each two
+// halves of n_mma fp32 columns: 2 for 64-wide heads, 1 for 128. With an even
+// count the two MMA threads take alternate stages: stages it and it - NA
+// then go to the same thread, whose own earlier wait keeps its parity waits
+// on that accumulator from running two phases ahead. With one accumulator a
+// single thread issues every stage.
+__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 2 : 1; }
 
-// TMEM columns per CTA: accumulators, then 4 scale columns per stage, then 4 for the query scales.
+// TMEM columns per CTA: accumulators, then 4 scale columns per stage half, then 4 for the query scales.
 __host__ __device__ constexpr int score_tmem_columns(int n_mma) {
-  return acc_buffers(n_mma) * n_mma + 4 * kScoreStages + 4 <= 256 ? 256 : 512;
+  return acc_buffers(n_mma) * kHalves * n_mma + 4 * kHalves * kScoreStages + 4 <= 256 ? 256 : 512;
 }
 constexpr int kTopkThreads = 512;
 constexpr int kExpandWarps = 8;
