@@ -664,8 +664,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (!ok) break;
         }
         const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
-        // an even accumulator count: alternate stages; otherwise the first thread issues all
-        if ((NA % 2 == 0) ? ((it & 1) == par) : (par == 0)) {
+        // several accumulators: alternate stages; one: the first thread issues all
+        if (NA > 1 ? ((it & 1) == par) : (par == 0)) {
           const int s = it % NS;
           const int a = it % NA;
           ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&

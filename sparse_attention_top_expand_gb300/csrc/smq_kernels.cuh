@@ -24,17 +24,20 @@ constexpr int kEpilogueThreads = 128;
 constexpr int kLoaderThreads = 128;
 constexpr int kScoreStages = 4;     // key stages resident in shared memory (32 KB each)
 constexpr int kLoadAhead = 3;       // stages each loader thread keeps in flight in registers
-constexpr int kMaxAccBuffers = 2;
+constexpr int kMaxAccBuffers = 3;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
 
 // TMEM accumulators in flight between the MMA and the epilogue, each two
-// halves of n_mma fp32 columns: 2 for 64-wide heads, 1 for 128. With an even
-// count the two MMA threads take alternate stages: stages it and it - NA
-// then go to the same thread, whose own earlier wait keeps its parity waits
-// on that accumulator from running two phases ahead. With one accumulator a
-// single thread issues every stage.
-__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 2 : 1; }
+// halves of n_mma fp32 columns: 3 for 64-wide heads, 1 for 128. With more
+// than one the two MMA threads take alternate stages. A parity wait on an
+// accumulator cannot pass a phase early: issuing stage it needs stage it to
+// be full, hence the epilogue past stage it - kScoreStages, hence (it works
+// in order) done reading stage it - 2 NA as long as kScoreStages < 2 NA. With
+// one accumulator a single thread issues every stage.
+__host__ __device__ constexpr int acc_buffers(int n_mma) { return n_mma <= 64 ? 3 : 1; }
+
+static_assert(kScoreStages < 2 * acc_buffers(64), "accumulator parity waits need kScoreStages < 2 NA");
 
 // TMEM columns per CTA: accumulators, then 4 scale columns per stage half, then 4 for the query scales.
 __host__ __device__ constexpr int score_tmem_columns(int n_mma) {
