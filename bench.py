@@ -300,8 +300,12 @@ def run_ours(args, rank, world, dist):
                                               d.row_indices, d.row_ke, d.candidate_blocks, d.topk_out,
                                               d.sparse_indices, d.end, d.workspace, profile_events=events)
 
-    # decode rows with at most 64 candidate blocks are expanded inside the score kernel
-    decode_launches = 2 if base.geom.candidate_topk_blocks <= 64 else 3
+    # decode rows with at most 64 candidate blocks are expanded inside the score kernel, which also
+    # selects their top-k when a row has at most 8448 sparse columns
+    if base.geom.candidate_topk_blocks <= 64:
+        decode_launches = 1 if plan.num_sparse_cols <= 8448 and 2 * rows <= plan.num_sms else 2
+    else:
+        decode_launches = 3
     launches_per_step = {"decode_batch": decode_launches, "long_context_decode": decode_launches,
                          "prefill_chunk": 4, "shared_schedule": 1 + 2 * len(layers)}[args.workload]
 
@@ -394,7 +398,8 @@ def run_ours(args, rank, world, dist):
             roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": load_traffic(args.workload, "score_kernel"),
                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": alg,
-                    "kernel": "score_kernel (fused gather + tcgen05 mxf8f6f4 + epilogue)"}
+                    "kernel": "score_kernel (fused expansion, gather, tcgen05 mxf8f6f4, epilogue"
+                              + (", top-k)" if decode_launches == 1 else ")")}
 
     cpu = run_cpu_baseline(args, base, rank) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 

@@ -126,11 +126,15 @@ SMQ_API int smq_plan_destroy(smq_plan *plan);
 SMQ_API int smq_plan_get_info(const smq_plan *plan, smq_plan_info *info);
 
 /* Device workspace bytes for calls of up to `rows` rows (<= max_rows).
- * It holds the status word, the fp32 logits scratch [rows][S] and the
- * schedule. Allocate it once, then zero it with smq_workspace_init. */
+ * It holds the status word, one tile counter per plan row (decode calls that
+ * expand their rows in the score kernel also select their top-k there; the
+ * counters find the CTA that finishes a row) and the fp32 logits scratch
+ * [rows][S]. Allocate it once, then zero it with smq_workspace_init. A call
+ * leaves the counters at zero; after a call whose status reports an error,
+ * zero the workspace again before the next call. */
 SMQ_API int smq_workspace_size(const smq_plan *plan, int32_t rows, size_t *bytes);
 
-/* Zero the workspace status word (async on stream). */
+/* Zero the workspace status word and tile counters (async on stream). */
 SMQ_API int smq_workspace_init(const smq_plan *plan, void *workspace, size_t workspace_bytes,
                                void *stream);
 
@@ -210,9 +214,10 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan *plan, const smq_decode
  * It does what sparse_mqa_logits_topk_decode does, with the same arguments,
  * except that args->workspace must be NULL and args->workspace_bytes 0. The
  * library uses its own scratch instead: a static device array of 256 bytes
- * plus 8 MiB (SMQ_NOALLOC_SCRATCH_BYTES) for the fp32 logits, held on every
- * GPU that loads the library until the process exits.
- *  - Rows * num_sparse_cols * 4 must not exceed 8 MiB, for example 256 rows
+ * plus 8 MiB (SMQ_NOALLOC_SCRATCH_BYTES) for the tile counters and the fp32
+ * logits, held on every GPU that loads the library until the process exits.
+ *  - The counters (4 bytes per plan row, rounded up to 256) plus
+ *    rows * num_sparse_cols * 4 must not exceed 8 MiB, for example 200 rows
  *    of 8192 columns. A larger call returns SMQ_ERR_WORKSPACE_TOO_SMALL and
  *    enqueues nothing.
  *  - The first call on a device looks up the scratch's device address
@@ -220,7 +225,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan *plan, const smq_decode
  *    before any stream capture.
  *  - Every call shares the one scratch: calls that overlap on the GPU (on
  *    different streams without ordering) race. Each call zeroes the scratch
- *    status word first.
+ *    status word and counters first.
  *  - Device-detected errors (bad page or row ids, timeouts) are recorded in
  *    the scratch and not returned. Callers who need them use
  *    sparse_mqa_logits_topk_decode with a workspace.

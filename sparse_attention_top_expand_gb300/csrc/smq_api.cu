@@ -69,8 +69,13 @@ int encode_q(CUtensorMap* m, const uint8_t* q, int64_t qrows, int n_mma) {
 
 constexpr size_t kStatusBytes = 256;
 
+// Workspace: [status word, 256 B][per-row tile counters, max_rows int32][fp32 logits, rows x num_cols].
+size_t counter_bytes(const smq_plan* p) {
+  return (static_cast<size_t>(p->desc.max_rows) * sizeof(int32_t) + 255) / 256 * 256;
+}
+
 size_t workspace_bytes_for(const smq_plan* p, int64_t rows) {
-  return kStatusBytes + static_cast<size_t>(rows) * p->num_cols * sizeof(float);
+  return kStatusBytes + counter_bytes(p) + static_cast<size_t>(rows) * p->num_cols * sizeof(float);
 }
 
 int check_device(smq_plan* p) {
@@ -148,8 +153,10 @@ smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a) {
   s.sparse_indices = a.sparse_indices;
   s.end = a.end;
   s.status = static_cast<int32_t*>(a.workspace);
+  s.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes);
   s.logits = a.logits_out ? a.logits_out
-                          : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes);
+                          : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes +
+                                                     counter_bytes(p));
   return s;
 }
 
@@ -198,9 +205,9 @@ int score_grid(const smq_plan* p, int rows) {
 // runtime whose device memory all belongs to its own pool and is not lent
 // out, or a plugin that may touch only the buffers it was handed. For them
 // the scratch is part of the loaded module, one copy on every device the
-// library is loaded on. Only the status word must start at zero (each call
-// clears it); the score kernel writes every logits column it covers before
-// top-k reads it.
+// library is loaded on. Only the status word and the per-row tile counters
+// must start at zero (each call clears them); the score kernel writes every
+// logits column it covers before top-k reads it.
 static __device__ __align__(256) uint8_t smq_noalloc_scratch[kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -310,8 +317,9 @@ SMQ_API int smq_workspace_size(const smq_plan* plan, int32_t rows, size_t* bytes
 }
 
 SMQ_API int smq_workspace_init(const smq_plan* plan, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!plan || !workspace || workspace_bytes < kStatusBytes) return SMQ_ERR_INVALID_ARG;
-  return cudaMemsetAsync(workspace, 0, kStatusBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  if (!plan || !workspace || workspace_bytes < kStatusBytes + counter_bytes(plan)) return SMQ_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, kStatusBytes + counter_bytes(plan), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? SMQ_OK
              : SMQ_ERR_CUDA;
 }
@@ -368,6 +376,18 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   record(a.profile_events[1], s);
   smq::ScoreParams sp = score_params(plan, c);
   sp.fused = fused ? 1 : 0;
+  // the score kernel also selects the top-k of the rows it expands when they are narrow enough
+  // and few enough that the CTA finishing a row rarely has a second one to select (a wide
+  // batch of rows is faster in the separate kernel, one CTA per row over every SM)
+  const bool fuse_topk = fused && plan->num_cols <= smq::kFusedTopkCols && 2 * a.rows <= plan->num_sms;
+  if (fuse_topk) {
+    sp.fused_topk = 1;
+    sp.topk = plan->desc.topk;
+    sp.topk_ld = a.topk_ld;
+    sp.topk_out = a.topk_out;
+    sp.col_indices = a.col_indices;
+    sp.logits_fill = a.logits_out;
+  }
   sp.ncb = plan->desc.candidate_topk_blocks;
   sp.cbs = plan->desc.candidate_block_size;
   sp.candidate_blocks = a.candidate_blocks;
@@ -385,7 +405,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
   if (smq::launch_score(sp, true, tm_q, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
-  rc = run_topk(plan, c, sp, s);
+  if (!fuse_topk) rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);
   return rc;
 }
@@ -462,16 +482,18 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const sm
   if (!plan || !args || args->struct_size < sizeof(smq_decode_args)) return SMQ_ERR_INVALID_ARG;
   if (args->workspace || args->workspace_bytes) return SMQ_ERR_INVALID_ARG;  // the library's scratch replaces it
   if (args->rows < 0 || args->rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
-  const size_t logits_bytes = static_cast<size_t>(args->rows) * plan->num_cols * sizeof(float);
-  if (logits_bytes > SMQ_NOALLOC_SCRATCH_BYTES) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes_for(plan, args->rows) > kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES)
+    return SMQ_ERR_WORKSPACE_TOO_SMALL;
   if (args->rows == 0) return SMQ_OK;
   int rc = check_device(const_cast<smq_plan*>(plan));  // the plan's device is current
   if (rc != SMQ_OK) return rc;
   void* scratch = nullptr;
   rc = noalloc_scratch(plan->desc.device, &scratch);
   if (rc != SMQ_OK) return rc;
-  // the kernels OR device-detected errors into the status word: start it at zero
-  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // the kernels OR device-detected errors into the status word and count finished
+  // tiles per row: start both at zero (a call that gave up may have left counts)
+  if (cudaMemsetAsync(scratch, 0, kStatusBytes + counter_bytes(plan), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return SMQ_ERR_CUDA;
   smq_decode_args a = *args;
   a.workspace = scratch;

@@ -43,6 +43,7 @@ namespace {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kE2M1 = 5, kE4M3 = 0;
+constexpr int32_t kRowDone = 0x40000000;  // flag on a row's end: this CTA selects the row's top-k
 
 __host__ __device__ constexpr uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -72,9 +73,9 @@ struct ScoreLayout {
     o += 2u * w_stride;
     meta = o;  // [2] {row, end, q_scale, unused}
     o += 2u * 16u;
-    bars = o;  // full, empty [stages]; acc_full, acc_empty [4]; q_full, q_empty [2]; drain [2];
-               // desc_full, desc_empty [ring]; setup copy
-    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing + 1u) * 8u, 16);
+    bars = o;  // full, empty [stages]; acc_full, acc_empty [accumulators]; q_full, q_empty [2]; drain [2];
+               // desc_full, desc_empty [ring]; setup copy; row stored
+    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing + 2u) * 8u, 16);
     misc = o;  // tmem base, abort flag
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
@@ -311,8 +312,187 @@ __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_
       si[slot] = v;
     }
     if (lane == 0) p.end_out[r] = static_cast<int32_t>(cols);
+    __threadfence();  // visible to the CTA that selects this row's top-k
   }
   return static_cast<int>(cols);
+}
+
+// ---------------------------------------------------------------------------
+// Top-k selection of one row by one CTA (used by topk_kernel and by the score
+// kernel for the rows it completes).
+// ---------------------------------------------------------------------------
+// Thread t holds the keys of columns t, t + T, t + 2T, ... in registers (T
+// threads). Up to four digit passes of 8 bits (most significant first) count
+// the keys that still match the selected prefix; the bin holding the k-th
+// largest key is found by a descending scan over the 256 bins. The histogram
+// keeps one copy per lane (bin b, copy l at word 32 b + l, bank l), so the
+// atomic increments of a warp never touch the same word or bank even when
+// most keys fall into a few bins, as logits do. The passes stop once every
+// key of the selected bin is taken. Then every key above the selected prefix,
+// and the first `need` keys inside it in column order, are written by one
+// ordered compaction: a single scan over the per-32-column counts gives each
+// warp its output offsets.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Shared memory of one row's selection.
+struct TopkScratch {
+  uint32_t* hist;    // [256 * 32], 16-byte aligned
+  int* bsum;         // [256]
+  int* wsum;         // [threads / 32]
+  uint32_t* chunk;   // [threads / 32 * kJ]
+  int32_t* sidx;     // [nsb]
+  int* sel;          // [12]
+};
+
+// Top-k of one row by the whole CTA. L: the row's S logits; end_src: where
+// the row's end is read (after the key loads are issued); sparse_row: the
+// row's sparse sub-block ids. Logits and ids may have been written by other
+// CTAs of the same kernel, so they are read from L2.
+template <int kThreads, int kJ>
+__device__ void select_topk(const float* L, int S, const int32_t* end_src, int k, const int32_t* sparse_row, int nsb,
+                            int sbkv, int32_t* out, int32_t* colo, float* fill, const TopkScratch& sm) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kBins = 256;
+  constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* hist = sm.hist;
+  int* sel_bin = sm.sel;
+  int* sel_above = sm.sel + 4;
+  int* sel_cnt = sm.sel + 8;
+  // the logits row has S columns whatever `end` is: load every key at once
+  float raw[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int c = tid + j * kThreads;
+    raw[j] = c < S ? __ldcg(L + c) : 0.f;
+  }
+  int e = *end_src;
+  e = e < 0 ? 0 : (e > S ? S : e);
+  for (int i = tid; i < nsb; i += kThreads) sm.sidx[i] = __ldcg(sparse_row + i);
+  uint4* hist4 = reinterpret_cast<uint4*>(hist);
+  for (int i = tid; i < kBins * 8; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+  if (fill)
+    for (int c = e + tid; c < S; c += kThreads) fill[c] = -INFINITY;
+  const int32_t* sidx = sm.sidx;
+  auto token = [&](int c) { return sidx[c / sbkv] * sbkv + c % sbkv; };
+  __syncthreads();
+  if (e <= k) {
+    for (int c = tid; c < k; c += kThreads) {
+      out[c] = c < e ? token(c) : -1;
+      if (colo) colo[c] = c < e ? c : -1;
+    }
+    return;
+  }
+  uint32_t key[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) key[j] = tid + j * kThreads < e ? ordered_key(raw[j]) : 0u;
+  uint32_t prefix = 0;  // selected high bits so far
+  int need = k;         // keys still to take among those matching the prefix
+  int done_bits = 0;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - done_bits;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = tid + j * kThreads;
+      const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
+      if (match) atomicAdd(&hist[((key[j] >> shift) & (kBins - 1)) * 32 + lane], 1u);
+    }
+    __syncthreads();
+    // bin totals: 32 copies each, read in a rotated order (no bank conflicts)
+    for (int b = tid; b < kBins; b += kThreads) {
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sum += static_cast<int>(hist[b * 32 + ((i + b) & 31)]);
+      sm.bsum[b] = sum;
+    }
+    __syncthreads();
+    // descending scan: thread t < 256 owns bin 255 - t
+    int cnt = 0, incl = 0;
+    if (tid < kBins) {
+      cnt = sm.bsum[kBins - 1 - tid];
+      incl = cnt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+    }
+    // every histogram read of this pass is done: clear it for the next one
+    for (int i = tid; i < kBins * 8; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (tid < kBins) {
+      int cum = incl - cnt;
+#pragma unroll
+      for (int w2 = 0; w2 < kBins / 32; ++w2) cum += w2 < warp ? sm.wsum[w2] : 0;  // independent loads
+      if (cnt > 0 && cum < need && need <= cum + cnt) {
+        sel_bin[pass] = kBins - 1 - tid;
+        sel_above[pass] = cum;
+        sel_cnt[pass] = cnt;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | static_cast<uint32_t>(sel_bin[pass]);
+    need -= sel_above[pass];
+    done_bits += 8;
+    if (need == sel_cnt[pass]) break;  // the whole bin is taken
+  }
+  // selected: keys whose top done_bits bits are above the prefix, and the
+  // first `need` of those equal to it, in column order
+  const uint32_t mask = ~0u << (32 - done_bits);
+  const uint32_t pfx = prefix << (32 - done_bits);
+  const int need_eq = need;
+  uint32_t bg[kJ], be[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int c = tid + j * kThreads;
+    bg[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) > pfx);
+    be[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) == pfx);
+    if (lane == 0) sm.chunk[j * kWarps + warp] = (static_cast<uint32_t>(__popc(bg[j])) << 16) | __popc(be[j]);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the packed counts (each half stays below 2^16)
+    constexpr int kPer = (kChunks + 31) / 32;
+    uint32_t v[kPer];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int c = lane * kPer + i;
+      v[i] = c < kChunks ? sm.chunk[c] : 0u;
+      sum += v[i];
+    }
+    uint32_t inc = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += t;
+    }
+    uint32_t run = inc - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int c = lane * kPer + i;
+      if (c < kChunks) sm.chunk[c] = run;
+      run += v[i];
+    }
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const uint32_t pre = sm.chunk[j * kWarps + warp];
+    const int c = tid + j * kThreads;
+    const bool gt = (bg[j] >> lane) & 1u, eq = (be[j] >> lane) & 1u;
+    const int pg = static_cast<int>(pre >> 16) + __popc(bg[j] & lt);
+    const int pe = static_cast<int>(pre & 0xffffu) + __popc(be[j] & lt);
+    int slot = -1;
+    if (gt) slot = pg + min(pe, need_eq);
+    else if (eq && pe < need_eq) slot = pg + pe;
+    if (slot >= 0 && slot < k) {
+      out[slot] = token(c);
+      if (colo) colo[slot] = c;
+    }
+  }
 }
 
 template <bool kPaged, int kN, bool kFused>
@@ -339,6 +519,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   auto bar_desc_full = [&](int d) { return smem_addr(&bars[NB + 6 + d]); };
   auto bar_desc_empty = [&](int d) { return smem_addr(&bars[NB + 6 + kDescRing + d]); };
   const uint32_t bar_setup = smem_addr(&bars[NB + 6 + 2 * kDescRing]);
+  const uint32_t bar_row_stored = smem_addr(&bars[NB + 7 + 2 * kDescRing]);  // epilogue warps, per row end
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + lay.scan);
@@ -367,6 +548,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain + 8, 1);
     mbar_init(bar_setup, 1);
+    mbar_init(bar_row_stored, kEpilogueThreads / 32);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -390,6 +572,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (kFused && nt == 0 && blockIdx.x == 0) {  // no column at all: CTA 0 writes the empty expansion
       for (int slot = 0; slot < p.nsb; ++slot) p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = -1;
       p.end_out[r] = 0;
+      if (p.fused_topk) {  // and the empty top-k
+        for (int c = 0; c < p.topk; ++c) {
+          p.topk_out[static_cast<int64_t>(r) * p.topk_ld + c] = -1;
+          if (p.col_indices) p.col_indices[static_cast<int64_t>(r) * p.topk + c] = -1;
+        }
+        if (p.logits_fill)
+          for (int c = 0; c < S; ++c) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
+      }
     }
   }
   int incl = mine;
@@ -705,6 +895,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     int r = find_row(prefix, R, t_begin);
     const int r_first = r;
     int cur = -1, qb = 0, row = 0, e = 0;
+    uint32_t nrow_ends = 0;
     bool need_end = false;
     uint32_t quse = 0;
     float qs = 0.f;
@@ -732,7 +923,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
       if (!ok) break;
       if (need_end) {  // written by the scheduler before it published this row's first tile
-        e = ld_volatile_s32(reinterpret_cast<const int32_t*>(smem + lay.rend) + (r - r_first));
+        e = ld_volatile_s32(reinterpret_cast<const int32_t*>(smem + lay.rend) + (r - r_first)) & ~kRowDone;
         need_end = false;
       }
       // the MMAs of this tile have finished: its key stage and scale columns are free
@@ -769,6 +960,30 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (last_of_row) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty(qb));
+        if constexpr (kFused) {
+          if (p.fused_topk) {
+            // this CTA's tiles of the row are stored: count them; the CTA that
+            // completes the row selects its top-k after the pipeline
+            if (lane == 0) mbar_arrive(bar_row_stored);
+            if (warp == 2 && lane == 0) {
+              if (mbar_wait(bar_row_stored, nrow_ends & 1, abort_flag, kWaitLimitNs)) {
+                const int64_t lo = prefix[r] > t_begin ? prefix[r] : t_begin;
+                const int64_t hi = prefix[r + 1] < t_end ? prefix[r + 1] : t_end;
+                const int mine = static_cast<int>(hi - lo), total = prefix[r + 1] - prefix[r];
+                __threadfence();
+                if (atomicAdd(p.row_done + r, mine) + mine == total) {
+                  p.row_done[r] = 0;  // ready for the next call
+                  __threadfence();
+                  st_volatile_s32(reinterpret_cast<int32_t*>(smem + lay.rend) + (r - r_first), e | kRowDone);
+                }
+              } else {
+                set_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
+              }
+            }
+            ++nrow_ends;
+          }
+        }
       }
     }
     if (!ok) {
@@ -878,177 +1093,65 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+
+  // ---- top-k of the rows this CTA completed (their logits are in L2) ----
+  if constexpr (kFused) {
+    if (p.fused_topk && *abort_flag == 0) {
+      uint8_t* scr = smem + lay.kv;  // the key stages are free now
+      TopkScratch sm;
+      sm.hist = reinterpret_cast<uint32_t*>(scr);
+      sm.bsum = reinterpret_cast<int*>(scr + 256 * 32 * 4);
+      sm.wsum = sm.bsum + 256;
+      sm.chunk = reinterpret_cast<uint32_t*>(sm.wsum + 32);
+      sm.sel = reinterpret_cast<int*>(sm.chunk + 32 * 32);
+      sm.sidx = sm.sel + 16;
+      const int32_t* rend = reinterpret_cast<const int32_t*>(smem + lay.rend);
+      const int r_first = find_row(prefix, R, t_begin);
+      for (int r = r_first; r < R && prefix[r] < t_end; ++r) {
+        if (prefix[r + 1] == prefix[r]) continue;
+        const int32_t* end_src = rend + (r - r_first);
+        if ((*end_src & kRowDone) == 0) continue;
+        int32_t* e_clean = sm.sel + 12;  // the end without the flag
+        if (tid == 0) *e_clean = *end_src & ~kRowDone;
+        __syncthreads();
+        const float* L = p.logits + static_cast<int64_t>(r) * S;
+        int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
+        int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr;
+        float* fill = p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr;
+        const int32_t* srow = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
+        if (S <= kScoreThreads * 11)
+          select_topk<kScoreThreads, 11>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+        else
+          select_topk<kScoreThreads, 22>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+        __syncthreads();  // the scratch is reused by the next row
+      }
+    }
+  }
 }
 
 // ===========================================================================
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
-// Thread t holds the keys of columns t, t + 512, t + 1024, ... in registers.
-// Up to four digit passes of 8 bits (most significant first) count the keys
-// that still match the selected prefix; the bin holding the k-th largest key
-// is found by a descending scan over the 256 bins. The histogram keeps one
-// copy per lane (bin b, copy l at word 32 b + l, bank l), so the atomic
-// increments of a warp never touch the same word or bank even when most keys
-// fall into a few bins, as logits do. The passes stop once every key of the
-// selected bin is taken. Then every key above the selected prefix, and the
-// first `need` keys inside it in column order, are written by one ordered
-// compaction: a single scan over the per-32-column counts gives each warp its
-// output offsets.
-__device__ __forceinline__ uint32_t ordered_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
+// One CTA per row (rows whose top-k the score kernel does not select itself).
 template <int kJ>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkParams p) {
   constexpr int kWarps = kTopkThreads / 32;
-  constexpr int kBins = 256;
-  constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
-  extern __shared__ int32_t sidx[];     // [nsb] sparse sub-block ids of the row
-  __shared__ __align__(16) uint32_t hist[kBins * 32];
-  __shared__ int bsum[kBins];
+  extern __shared__ int32_t sidx[];  // [nsb] sparse sub-block ids of the row
+  __shared__ __align__(16) uint32_t hist[256 * 32];
+  __shared__ int bsum[256];
   __shared__ int wsum[kWarps];
-  __shared__ uint32_t chunk_cnt[kChunks];  // (above << 16) | inside, then their exclusive prefix
-  __shared__ int sel_bin[4], sel_above[4], sel_cnt[4];
+  __shared__ uint32_t chunk[kWarps * kJ];
+  __shared__ int sel[12];
   griddep_launch_dependents();
   griddep_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   const int S = p.num_cols;
-  const int k = p.topk;
-  const int sbkv = p.sbkv;
-  const float* L = p.logits + static_cast<int64_t>(r) * S;
-  // the logits row has S columns whatever `end` is: load every key at once
-  float raw[kJ];
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const int c = tid + j * kTopkThreads;
-    raw[j] = c < S ? L[c] : 0.f;
-  }
-  int e = p.end[r];
-  e = e < 0 ? 0 : (e > S ? S : e);
-  for (int i = tid; i < p.nsb; i += kTopkThreads) sidx[i] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + i];
-  uint4* hist4 = reinterpret_cast<uint4*>(hist);
-  for (int i = tid; i < kBins * 8; i += kTopkThreads) hist4[i] = make_uint4(0, 0, 0, 0);
-  if (p.logits_fill)
-    for (int c = e + tid; c < S; c += kTopkThreads) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
-  int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
-  int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * k : nullptr;
-  auto token = [&](int c) { return sidx[c / sbkv] * sbkv + c % sbkv; };
-  __syncthreads();
-  if (e <= k) {
-    for (int c = tid; c < k; c += kTopkThreads) {
-      out[c] = c < e ? token(c) : -1;
-      if (colo) colo[c] = c < e ? c : -1;
-    }
-    return;
-  }
-  uint32_t key[kJ];
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) key[j] = tid + j * kTopkThreads < e ? ordered_key(raw[j]) : 0u;
-  uint32_t prefix = 0;  // selected high bits so far
-  int need = k;         // keys still to take among those matching the prefix
-  int done_bits = 0;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - done_bits;
-#pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const int c = tid + j * kTopkThreads;
-      const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
-      if (match) atomicAdd(&hist[((key[j] >> shift) & (kBins - 1)) * 32 + lane], 1u);
-    }
-    __syncthreads();
-    {  // bin totals: two threads per bin, 16 copies each, read in a rotated order (no bank conflicts)
-      const int b = tid >> 1, h = tid & 1;
-      int sum = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sum += static_cast<int>(hist[b * 32 + ((h * 16 + i + b) & 31)]);
-      sum += __shfl_xor_sync(kFullMask, sum, 1);
-      if (h == 0) bsum[b] = sum;
-    }
-    __syncthreads();
-    // descending scan: thread t < 256 owns bin 255 - t
-    int cnt = 0, incl = 0;
-    if (tid < kBins) {
-      cnt = bsum[kBins - 1 - tid];
-      incl = cnt;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFullMask, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (lane == 31) wsum[warp] = incl;
-    }
-    // every histogram read of this pass is done: clear it for the next one
-    for (int i = tid; i < kBins * 8; i += kTopkThreads) hist4[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    if (tid < kBins) {
-      int cum = incl - cnt;
-#pragma unroll
-      for (int w2 = 0; w2 < kBins / 32; ++w2) cum += w2 < warp ? wsum[w2] : 0;  // independent loads
-      if (cnt > 0 && cum < need && need <= cum + cnt) {
-        sel_bin[pass] = kBins - 1 - tid;
-        sel_above[pass] = cum;
-        sel_cnt[pass] = cnt;
-      }
-    }
-    __syncthreads();
-    prefix = (prefix << 8) | static_cast<uint32_t>(sel_bin[pass]);
-    need -= sel_above[pass];
-    done_bits += 8;
-    if (need == sel_cnt[pass]) break;  // the whole bin is taken
-  }
-  // selected: keys whose top done_bits bits are above the prefix, and the
-  // first `need` of those equal to it, in column order
-  const uint32_t mask = ~0u << (32 - done_bits);
-  const uint32_t pfx = prefix << (32 - done_bits);
-  const int need_eq = need;
-  uint32_t bg[kJ], be[kJ];
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const int c = tid + j * kTopkThreads;
-    bg[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) > pfx);
-    be[j] = __ballot_sync(kFullMask, c < e && (key[j] & mask) == pfx);
-    if (lane == 0) chunk_cnt[j * kWarps + warp] = (static_cast<uint32_t>(__popc(bg[j])) << 16) | __popc(be[j]);
-  }
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of the packed counts (each half stays below 2^16)
-    constexpr int kPer = kChunks / 32;
-    uint32_t v[kPer];
-    uint32_t sum = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      v[i] = chunk_cnt[lane * kPer + i];
-      sum += v[i];
-    }
-    uint32_t inc = sum;
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(kFullMask, inc, o);
-      if (lane >= o) inc += t;
-    }
-    uint32_t run = inc - sum;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      chunk_cnt[lane * kPer + i] = run;
-      run += v[i];
-    }
-  }
-  __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const uint32_t pre = chunk_cnt[j * kWarps + warp];
-    const int c = tid + j * kTopkThreads;
-    const bool gt = (bg[j] >> lane) & 1u, eq = (be[j] >> lane) & 1u;
-    const int pg = static_cast<int>(pre >> 16) + __popc(bg[j] & lt);
-    const int pe = static_cast<int>(pre & 0xffffu) + __popc(be[j] & lt);
-    int slot = -1;
-    if (gt) slot = pg + min(pe, need_eq);
-    else if (eq && pe < need_eq) slot = pg + pe;
-    if (slot >= 0 && slot < k) {
-      out[slot] = token(c);
-      if (colo) colo[slot] = c;
-    }
-  }
+  const TopkScratch sm{hist, bsum, wsum, chunk, sidx, sel};
+  select_topk<kTopkThreads, kJ>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
+                                p.sparse_indices + static_cast<int64_t>(r) * p.nsb, p.nsb, p.sbkv,
+                                p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
+                                p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr,
+                                p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr, sm);
 }
 
 // ===========================================================================

@@ -44,6 +44,7 @@ __host__ __device__ constexpr int score_tmem_columns(int n_mma) {
   return acc_buffers(n_mma) * kHalves * n_mma + 4 * kHalves * kScoreStages + 4 <= 256 ? 256 : 512;
 }
 constexpr int kTopkThreads = 512;
+constexpr int kFusedTopkCols = kScoreThreads * 22;  // widest row the score kernel selects itself
 constexpr int kExpandWarps = 8;
 constexpr int kMaxRowsPerCall = 8192;
 constexpr int kMaxSparseCols = 16384;
@@ -88,6 +89,15 @@ struct ScoreParams {
   const int32_t* row_ke;
   int32_t* sparse_indices_out;
   int32_t* end_out;
+  // top-k selected in the score kernel (rows expanded here, num_cols <= kFusedTopkCols): the CTA
+  // that finishes a row's last tile, counted in row_done, selects that row after its pipeline
+  int32_t fused_topk;
+  int32_t topk;
+  int32_t topk_ld;
+  int32_t* row_done;     // [rows] finished tiles per row; zero before a call, left zero after it
+  int32_t* topk_out;     // [rows][topk_ld]
+  int32_t* col_indices;  // [rows][topk], may be null
+  float* logits_fill;    // when non-null: -inf into columns >= end (the caller's logits_out)
   // outputs
   float* logits;     // [rows][num_cols]
   int32_t* status;   // workspace status word

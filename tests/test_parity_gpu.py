@@ -202,3 +202,17 @@ def test_repeat_calls_are_deterministic():
     dev.run(plan)
     _ok(smq.smq_get_status(dev.workspace))
     assert torch.equal(first[0], dev.topk_out) and torch.equal(first[1], dev.logits)
+
+
+def test_tile_counters_are_left_at_zero():
+    """Rows whose top-k the score kernel selects count finished tiles in the
+    workspace; a call leaves those counters at zero for the next call."""
+    inp = synth.decode_batch(rows=16)
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    counters = dev.workspace[256:256 + 4 * plan.max_rows].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
+    dev.run(plan)
+    _ok(smq.smq_get_status(dev.workspace))
+    assert int(counters.abs().sum()) == 0
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, rows=[0, 5, 15], mode="sparse"))
