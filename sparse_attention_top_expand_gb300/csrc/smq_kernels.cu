@@ -322,25 +322,31 @@ __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_
 // kernel for the rows it completes).
 // ---------------------------------------------------------------------------
 // Thread t holds the keys of columns t, t + T, t + 2T, ... in registers (T
-// threads). Up to four digit passes of 8 bits (most significant first) count
-// the keys that still match the selected prefix; the bin holding the k-th
-// largest key is found by a descending scan over the 256 bins. The histogram
-// keeps one copy per lane (bin b, copy l at word 32 b + l, bank l), so the
-// atomic increments of a warp never touch the same word or bank even when
-// most keys fall into a few bins, as logits do. The passes stop once every
-// key of the selected bin is taken. Then every key above the selected prefix,
-// and the first `need` keys inside it in column order, are written by one
-// ordered compaction: a single scan over the per-32-column counts gives each
-// warp its output offsets.
+// threads). Digit passes (most significant first) count the keys that still
+// match the selected prefix; the bin holding the k-th largest key is found by
+// a descending scan. Two schemes:
+//  - 12, 12 and 8 bits in a 4096-bin histogram, thread t scanning a run of
+//    consecutive bins and clearing them once read. Logits spread over the top
+//    12 bits (sign, exponent, three mantissa bits), so a warp's increments
+//    rarely meet in one bin, and two passes usually suffice (the score
+//    kernel's own selection).
+//  - four 8-bit passes over 256 bins with one copy per lane, which needs fewer
+//    registers (the separate kernel, where occupancy matters).
+// The passes stop once every key of the selected bin is taken.
+// Then every key above the selected prefix, and the first `need` keys inside
+// it in column order, are written by one ordered compaction: a single scan
+// over the per-32-column counts gives each warp its output offsets.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kTopkBins = 4096;
+
 // Shared memory of one row's selection.
 struct TopkScratch {
-  uint32_t* hist;    // [256 * 32], 16-byte aligned
-  int* bsum;         // [256]
+  uint32_t* hist;    // [kTopkBins] (12-bit digits) or [256 * 32] (8-bit digits, a copy per lane), 16-byte aligned
+  int* bsum;         // [256] (8-bit digits)
   int* wsum;         // [threads / 32]
   uint32_t* chunk;   // [threads / 32 * kJ]
   int32_t* sidx;     // [nsb]
@@ -351,12 +357,12 @@ struct TopkScratch {
 // the row's end is read (after the key loads are issued); sparse_row: the
 // row's sparse sub-block ids. Logits and ids may have been written by other
 // CTAs of the same kernel, so they are read from L2.
-template <int kThreads, int kJ>
+template <int kThreads, int kJ, bool kWide>
 __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k, const int32_t* sparse_row, int nsb,
                             int sbkv, int32_t* out, int32_t* colo, float* fill, const TopkScratch& sm) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kBins = 256;
   constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
+  constexpr int kPerThread = (kTopkBins + kThreads - 1) / kThreads;  // bins a thread scans
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* hist = sm.hist;
   int* sel_bin = sm.sel;
@@ -373,7 +379,7 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   e = e < 0 ? 0 : (e > S ? S : e);
   for (int i = tid; i < nsb; i += kThreads) sm.sidx[i] = __ldcg(sparse_row + i);
   uint4* hist4 = reinterpret_cast<uint4*>(hist);
-  for (int i = tid; i < kBins * 8; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (kWide ? kTopkBins : 256 * 32) / 4; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
   if (fill)
     for (int c = e + tid; c < S; c += kThreads) fill[c] = -INFINITY;
   const int32_t* sidx = sm.sidx;
@@ -392,27 +398,79 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   uint32_t prefix = 0;  // selected high bits so far
   int need = k;         // keys still to take among those matching the prefix
   int done_bits = 0;
+  if constexpr (kWide) {
+  for (int pass = 0; pass < 3; ++pass) {
+    const int wbits = pass < 2 ? 12 : 8;
+    const int nb = 1 << wbits;
+    const int shift = 32 - done_bits - wbits;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = tid + j * kThreads;
+      const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
+      if (match) atomicAdd(&hist[(key[j] >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    // descending scan: thread t owns bins nb - 1 - per t - b for b < per
+    const int per = (nb + kThreads - 1) / kThreads;
+    int cnt[kPerThread];
+    int local = 0;
+#pragma unroll
+    for (int b = 0; b < kPerThread; ++b) {
+      const int bin = nb - 1 - per * tid - b;
+      cnt[b] = 0;
+      if (b < per && bin >= 0) {
+        cnt[b] = static_cast<int>(hist[bin]);
+        hist[bin] = 0;  // read once, cleared for the next pass
+      }
+      local += cnt[b];
+    }
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.wsum[warp] = incl;
+    __syncthreads();
+    int cum = incl - local;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) cum += w2 < warp ? sm.wsum[w2] : 0;  // independent loads
+#pragma unroll
+    for (int b = 0; b < kPerThread; ++b) {
+      if (cnt[b] > 0 && cum < need && need <= cum + cnt[b]) {
+        sel_bin[pass] = nb - 1 - per * tid - b;
+        sel_above[pass] = cum;
+        sel_cnt[pass] = cnt[b];
+      }
+      cum += cnt[b];
+    }
+    __syncthreads();
+    prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin[pass]);
+    need -= sel_above[pass];
+    done_bits += wbits;
+    if (need == sel_cnt[pass]) break;  // the whole bin is taken
+  }
+  } else {
+  // four 8-bit passes over a 256-bin histogram with one copy per lane (bin b,
+  // copy l at word 32 b + l, bank l): a warp's increments never meet
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - done_bits;
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int c = tid + j * kThreads;
       const bool match = c < e && (done_bits == 0 || (key[j] >> (32 - done_bits)) == prefix);
-      if (match) atomicAdd(&hist[((key[j] >> shift) & (kBins - 1)) * 32 + lane], 1u);
+      if (match) atomicAdd(&hist[((key[j] >> shift) & 255) * 32 + lane], 1u);
     }
     __syncthreads();
-    // bin totals: 32 copies each, read in a rotated order (no bank conflicts)
-    for (int b = tid; b < kBins; b += kThreads) {
+    for (int b = tid; b < 256; b += kThreads) {  // bin totals, copies read in a rotated order
       int sum = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) sum += static_cast<int>(hist[b * 32 + ((i + b) & 31)]);
       sm.bsum[b] = sum;
     }
     __syncthreads();
-    // descending scan: thread t < 256 owns bin 255 - t
-    int cnt = 0, incl = 0;
-    if (tid < kBins) {
-      cnt = sm.bsum[kBins - 1 - tid];
+    int cnt = 0, incl = 0;  // descending scan: thread t < 256 owns bin 255 - t
+    if (tid < 256) {
+      cnt = sm.bsum[255 - tid];
       incl = cnt;
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(kFullMask, incl, o);
@@ -420,15 +478,14 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
       }
       if (lane == 31) sm.wsum[warp] = incl;
     }
-    // every histogram read of this pass is done: clear it for the next one
-    for (int i = tid; i < kBins * 8; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 256 * 8; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);  // read: clear for the next pass
     __syncthreads();
-    if (tid < kBins) {
+    if (tid < 256) {
       int cum = incl - cnt;
 #pragma unroll
-      for (int w2 = 0; w2 < kBins / 32; ++w2) cum += w2 < warp ? sm.wsum[w2] : 0;  // independent loads
+      for (int w2 = 0; w2 < 8; ++w2) cum += w2 < warp ? sm.wsum[w2] : 0;
       if (cnt > 0 && cum < need && need <= cum + cnt) {
-        sel_bin[pass] = kBins - 1 - tid;
+        sel_bin[pass] = 255 - tid;
         sel_above[pass] = cum;
         sel_cnt[pass] = cnt;
       }
@@ -438,6 +495,7 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
     need -= sel_above[pass];
     done_bits += 8;
     if (need == sel_cnt[pass]) break;  // the whole bin is taken
+  }
   }
   // selected: keys whose top done_bits bits are above the prefix, and the
   // first `need` of those equal to it, in column order
@@ -1100,8 +1158,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       uint8_t* scr = smem + lay.kv;  // the key stages are free now
       TopkScratch sm;
       sm.hist = reinterpret_cast<uint32_t*>(scr);
-      sm.bsum = reinterpret_cast<int*>(scr + 256 * 32 * 4);
-      sm.wsum = sm.bsum + 256;
+      sm.bsum = nullptr;
+      sm.wsum = reinterpret_cast<int*>(scr + kTopkBins * 4);
       sm.chunk = reinterpret_cast<uint32_t*>(sm.wsum + 32);
       sm.sel = reinterpret_cast<int*>(sm.chunk + 32 * 32);
       sm.sidx = sm.sel + 16;
@@ -1120,9 +1178,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         float* fill = p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr;
         const int32_t* srow = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
         if (S <= kScoreThreads * 11)
-          select_topk<kScoreThreads, 11>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+          select_topk<kScoreThreads, 11, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
         else
-          select_topk<kScoreThreads, 22>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+          select_topk<kScoreThreads, 22, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
         __syncthreads();  // the scratch is reused by the next row
       }
     }
@@ -1133,8 +1191,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
 // One CTA per row (rows whose top-k the score kernel does not select itself).
+// Rows are many and each CTA is latency bound, so the launch bound keeps 3,
+// 2 or 1 CTAs per SM resident (at most 42, 64 or 128 registers a thread).
 template <int kJ>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkParams p) {
+__global__ void __launch_bounds__(kTopkThreads, kJ <= 8 ? 3 : (kJ <= 16 ? 2 : 1))
+    topk_kernel(const __grid_constant__ TopkParams p) {
   constexpr int kWarps = kTopkThreads / 32;
   extern __shared__ int32_t sidx[];  // [nsb] sparse sub-block ids of the row
   __shared__ __align__(16) uint32_t hist[256 * 32];
@@ -1147,7 +1208,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   const int r = blockIdx.x;
   const int S = p.num_cols;
   const TopkScratch sm{hist, bsum, wsum, chunk, sidx, sel};
-  select_topk<kTopkThreads, kJ>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
+  select_topk<kTopkThreads, kJ, false>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
                                 p.sparse_indices + static_cast<int64_t>(r) * p.nsb, p.nsb, p.sbkv,
                                 p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
                                 p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr,
