@@ -101,7 +101,8 @@ typedef struct smq_plan_desc {
   int32_t candidate_block_size;  /* cbs > 0 */
   int32_t candidate_topk_blocks; /* ncb > 0 candidate blocks per row */
   int32_t topk;                  /* k: 1 <= k <= num_sparse_cols, k <= 16384 */
-  int32_t sparse_block_kv;       /* sub-block size in tokens; 0 picks the largest of
+  int32_t sparse_block_kv;       /* sub-block size in tokens: 16, 32, 64 or 128 (else
+                                    SMQ_ERR_UNSUPPORTED); 0 picks the largest of
                                     128/64/32/16 dividing both page_size and cbs */
   int32_t max_rows;              /* upper bound on rows per call (workspace sizing), <= 8192 */
   int32_t device;                /* CUDA device ordinal the plan runs on */

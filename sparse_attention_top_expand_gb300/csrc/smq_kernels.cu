@@ -184,6 +184,21 @@ __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_
 // Global -> shared loads on the LSU path (the key rows of a tile come from
 // scattered pages; many independent 16-byte loads keep far more bytes in
 // flight per SM than the tensor-copy engine did for 64-byte rows).
+// The same loads under a predicate (no branch): where pred is false nothing
+// is read and v keeps its value.
+__device__ __forceinline__ void ldg_stream_v4_if(uint4& v, const void* p, bool pred) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n @q ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n}"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "l"(p), "r"(pred ? 1 : 0));
+}
+
+__device__ __forceinline__ void ldg_stream_u32_if(uint32_t& v, const void* p, bool pred) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.L1::no_allocate.u32 %0, [%1];\n}"
+               : "+r"(v)
+               : "l"(p), "r"(pred ? 1 : 0));
+}
+
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -240,6 +255,23 @@ __device__ __forceinline__ int32_t ld_volatile_s32(const int32_t* a) {
   int32_t v;
   asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(a)) : "memory");
   return v;
+}
+
+// Loads one word and drops it. Issued early for buffers that are written
+// much later, so that their address translation is cached by then (a cold
+// miss stalls the stores that hit it for microseconds).
+__device__ __forceinline__ void touch_global(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+}
+
+// Adds with release and acquire semantics at GPU scope: this thread's
+// earlier writes (and those it acquired) are visible before the add, and
+// writes released by the adds it observes are visible after it.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 // Candidate expansion of row r by one warp, for at most 64 candidate blocks
@@ -383,7 +415,8 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   if (fill)
     for (int c = e + tid; c < S; c += kThreads) fill[c] = -INFINITY;
   const int32_t* sidx = sm.sidx;
-  auto token = [&](int c) { return sidx[c / sbkv] * sbkv + c % sbkv; };
+  const int sb_shift = 31 - __clz(sbkv);  // the sub-block size is a power of two (16..128)
+  auto token = [&](int c) { return (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1)); };
   __syncthreads();
   if (e <= k) {
     for (int c = tid; c < k; c += kThreads) {
@@ -952,6 +985,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     int r = find_row(prefix, R, t_begin);
     const int r_first = r;
+    if constexpr (kFused) {
+      if (p.fused_topk) {  // rows this CTA may select: warm the translations of their outputs
+        const int rr = r_first + (tid - 2 * 32);
+        if (rr < R && prefix[rr] < t_end && prefix[rr + 1] > prefix[rr]) {
+          touch_global(p.topk_out + static_cast<int64_t>(rr) * p.topk_ld);
+          touch_global(p.sparse_indices_out + static_cast<int64_t>(rr) * p.nsb);
+          touch_global(p.logits + static_cast<int64_t>(rr) * S);
+          touch_global(p.row_done + rr);
+        }
+      }
+    }
     int cur = -1, qb = 0, row = 0, e = 0;
     uint32_t nrow_ends = 0;
     bool need_end = false;
@@ -1028,10 +1072,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const int64_t lo = prefix[r] > t_begin ? prefix[r] : t_begin;
                 const int64_t hi = prefix[r + 1] < t_end ? prefix[r + 1] : t_end;
                 const int mine = static_cast<int>(hi - lo), total = prefix[r + 1] - prefix[r];
-                __threadfence();
-                if (atomicAdd(p.row_done + r, mine) + mine == total) {
+                // release: the logits the epilogue warps stored (acquired through the barrier);
+                // acquire: those of the CTAs whose counts this add observes
+                if (atom_add_acq_rel_gpu(p.row_done + r, mine) + mine == total) {
                   p.row_done[r] = 0;  // ready for the next call
-                  __threadfence();
                   st_volatile_s32(reinterpret_cast<int32_t*>(smem + lay.rend) + (r - r_first), e | kRowDone);
                 }
               } else {
@@ -1078,9 +1122,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t kv_base = smem_addr(smem + lay.kv);
     uint4 v[kLoadAhead][kChunks];
     uint32_t sw[kLoadAhead][kHalves];
-    uint32_t have[kLoadAhead];  // bit k8: value chunk k8 was loaded
 #pragma unroll
-    for (int k = 0; k < kLoadAhead; ++k) have[k] = 0;
+    for (int k = 0; k < kLoadAhead; ++k) {
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) v[k][k8] = make_uint4(0u, 0u, 0u, 0u);
+    }
     bool ok = true;
     for (int i0 = 0; i0 < n + kLoadAhead && ok; i0 += kLoadAhead) {
 #pragma unroll
@@ -1095,13 +1141,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
 #pragma unroll
           for (int k8 = 0; k8 < kChunks; ++k8) {
-            if (have[k] & (1u << k8)) {
-              const int pos = (m >> 2) + 32 * k8;
-              const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
-              const uint32_t swz = static_cast<uint32_t>(pos & 7);
-              sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k8].x, v[k][k8].y);
-              sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k8].z, v[k][k8].w);
-            }
+            // stored whether or not the chunk was loaded: an unloaded chunk holds
+            // an older key's bytes (finite E2M1 values, scale 1) in a position the
+            // epilogue never stores
+            const int pos = (m >> 2) + 32 * k8;
+            const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
+            const uint32_t swz = static_cast<uint32_t>(pos & 7);
+            sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k8].x, v[k][k8].y);
+            sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k8].z, v[k][k8].w);
           }
           // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
           // half's block, which the copy to TMEM places at lane m, column base + m / 32
@@ -1116,22 +1163,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           const SubBlockSrc* dring = desc + dslot * kMaxSubsPerTile;
-          uint32_t hv = 0;
+          // predicated loads: a branch per chunk costs more than the load
 #pragma unroll
           for (int k8 = 0; k8 < kChunks; ++k8) {
             const SubBlockSrc d = get_src(dring + vu[k8]);
-            if (d.values != nullptr && vtk[k8] < d.positions) {
-              v[k][k8] = ldg_stream_v4(d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch);
-              hv |= 1u << k8;
-            }
+            ldg_stream_v4_if(v[k][k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
+                             d.values != nullptr && vtk[k8] < d.positions);
           }
-          have[k] = hv;
 #pragma unroll
           for (int h = 0; h < kHalves; ++h) {
             const SubBlockSrc ds = get_src(dring + su[h]);
-            sw[k][h] = 0x7F7F7F7Fu;
-            if (ds.values != nullptr && stk[h] < ds.positions)
-              sw[k][h] = ldg_stream_u32(ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes);
+            sw[k][h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
+            ldg_stream_u32_if(sw[k][h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
+                              ds.values != nullptr && stk[h] < ds.positions);
           }
           __syncwarp();  // every lane has read the entries before they are handed back
           if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
@@ -1144,13 +1188,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   }
 
-  // ---- teardown ----
+  // ---- teardown (TMEM is freed at the very end, so the top-k tail need not wait for it) ----
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, p.tmem_cols);
-  }
 
   // ---- top-k of the rows this CTA completed (their logits are in L2) ----
   if constexpr (kFused) {
@@ -1184,6 +1224,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         __syncthreads();  // the scratch is reused by the next row
       }
     }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
   }
 }
 

@@ -23,7 +23,7 @@ constexpr int kMmaWarp1 = 11;       // second MMA issuer (odd tiles); warp 1 iss
 constexpr int kEpilogueThreads = 128;
 constexpr int kLoaderThreads = 128;
 constexpr int kScoreStages = 4;     // key stages resident in shared memory (32 KB each)
-constexpr int kLoadAhead = 3;       // stages each loader thread keeps in flight in registers
+constexpr int kLoadAhead = 2;       // stages each loader thread keeps in flight in registers
 constexpr int kMaxAccBuffers = 3;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
