@@ -222,9 +222,10 @@ __device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
 }
 
 // The address ring is shared between warps that hand entries back and forth
-// through mbarriers. Its reads and writes are volatile shared accesses, so
-// that the compiler neither delays them past the hand-off nor repeats a read
-// after the entry has been handed back and rewritten.
+// through mbarriers. Writes are volatile shared stores. Reads are plain loads
+// between the reader's mbarrier wait and its hand-back arrival: both are
+// compiler memory barriers, so no read moves out of that window, and the
+// compiler is free to merge and schedule the reads inside it.
 __device__ __forceinline__ void put_src(SubBlockSrc* e, const uint8_t* values, const uint8_t* scales, int positions) {
   const uint32_t a = smem_addr(e);
   asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a), "l"(values) : "memory");
@@ -233,18 +234,7 @@ __device__ __forceinline__ void put_src(SubBlockSrc* e, const uint8_t* values, c
 }
 
 __device__ __forceinline__ SubBlockSrc get_src(const SubBlockSrc* e) {
-  const uint32_t a = smem_addr(e);
-  uint64_t v, sc;
-  int32_t n;
-  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
-  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(sc) : "r"(a + 8) : "memory");
-  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(n) : "r"(a + 16) : "memory");
-  SubBlockSrc d;
-  d.values = reinterpret_cast<const uint8_t*>(v);
-  d.scales = reinterpret_cast<const uint8_t*>(sc);
-  d.positions = n;
-  d.pad = 0;
-  return d;
+  return *e;
 }
 
 __device__ __forceinline__ void st_volatile_s32(int32_t* a, int32_t v) {
@@ -1127,58 +1117,86 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
       for (int k8 = 0; k8 < kChunks; ++k8) v[k][k8] = make_uint4(0u, 0u, 0u, 0u);
     }
+    // Tiles go in pairs: slot k holds tile i0 + k. A wait costs a warp about
+    // as much as a tile's stores, so each pair takes one `empty` wait (stages
+    // are freed in tile order: the later one implies the earlier) and, once
+    // the ring runs ahead, one descriptor wait (published in tile order).
+    static_assert(kLoadAhead == 2, "the loader works on pairs of tiles");
+    auto store_tile = [&](const uint4 (&vv)[kChunks], const uint32_t (&ss)[kHalves], int j) {
+      const int s = j % NS;
+      const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) {
+        // stored whether or not the chunk was loaded: an unloaded chunk holds
+        // an older key's bytes (finite E2M1 values, scale 1) in a position the
+        // epilogue never stores
+        const int pos = (m >> 2) + 32 * k8;
+        const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
+        const uint32_t swz = static_cast<uint32_t>(pos & 7);
+        sts_v2(dst + (((2 * vch) ^ swz) << 4), vv[k8].x, vv[k8].y);
+        sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), vv[k8].z, vv[k8].w);
+      }
+      // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
+      // half's block, which the copy to TMEM places at lane m, column base + m / 32
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
+      fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
+      __syncwarp();              // one arrival per warp
+      if (lane == 0) mbar_arrive(bar_full(s));
+    };
+    auto load_tile = [&](uint4 (&vv)[kChunks], uint32_t (&ss)[kHalves], int i) {
+      const SubBlockSrc* dring = desc + (i % kDescRing) * kMaxSubsPerTile;
+      // predicated loads: a branch per chunk costs more than the load
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) {
+        const SubBlockSrc d = get_src(dring + vu[k8]);
+        ldg_stream_v4_if(vv[k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
+                         d.values != nullptr && vtk[k8] < d.positions);
+      }
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        const SubBlockSrc ds = get_src(dring + su[h]);
+        ss[h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
+        ldg_stream_u32_if(ss[h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
+                          ds.values != nullptr && stk[h] < ds.positions);
+      }
+    };
     bool ok = true;
-    for (int i0 = 0; i0 < n + kLoadAhead && ok; i0 += kLoadAhead) {
-#pragma unroll
-      for (int k = 0; k < kLoadAhead; ++k) {
-        const int i = i0 + k;
-        const int j = i - kLoadAhead;  // the stage whose data sits in slot k
-        if (j >= 0 && j < n) {
-          const int s = j % NS;
-          // the stage is free once the MMAs of stage j - NS have finished
-          ok = warp_wait(bar_empty(s), ((j / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+    for (int i0 = 0; i0 < n + 2; i0 += 2) {
+      const int j0 = i0 - 2;  // the pair whose data sits in the slots
+      if (j0 >= 0 && j0 < n) {
+        const int jl = j0 + 1 < n ? j0 + 1 : j0;
+        // the stages are free once the MMAs of tiles j0 - NS and jl - NS have finished
+        ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        store_tile(v[0], sw[0], j0);
+        if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
+      }
+      if (i0 < n) {
+        // when the pair's second tile is already published (the ring runs ahead),
+        // nothing is waited for; otherwise each tile is waited for, so that the
+        // first loads leave as soon as their tile is published
+        const int il = i0 + 1 < n ? i0 + 1 : i0;
+        bool both = false;
+        if (lane == 0) both = mbar_test_wait(bar_desc_full(il % kDescRing), (il / kDescRing) & 1);
+        both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
+        __syncwarp();  // orders the other lanes after lane 0's acquire
+        if (!both) {
+          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
-          const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
-#pragma unroll
-          for (int k8 = 0; k8 < kChunks; ++k8) {
-            // stored whether or not the chunk was loaded: an unloaded chunk holds
-            // an older key's bytes (finite E2M1 values, scale 1) in a position the
-            // epilogue never stores
-            const int pos = (m >> 2) + 32 * k8;
-            const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
-            const uint32_t swz = static_cast<uint32_t>(pos & 7);
-            sts_v2(dst + (((2 * vch) ^ swz) << 4), v[k][k8].x, v[k][k8].y);
-            sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), v[k][k8].z, v[k][k8].w);
-          }
-          // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
-          // half's block, which the copy to TMEM places at lane m, column base + m / 32
-#pragma unroll
-          for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, sw[k][h]);
-          fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
-          __syncwarp();  // one arrival per warp
-          if (lane == 0) mbar_arrive(bar_full(s));
         }
-        if (i < n) {
-          const int dslot = i % kDescRing;
-          ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
-          if (!ok) break;
-          const SubBlockSrc* dring = desc + dslot * kMaxSubsPerTile;
-          // predicated loads: a branch per chunk costs more than the load
-#pragma unroll
-          for (int k8 = 0; k8 < kChunks; ++k8) {
-            const SubBlockSrc d = get_src(dring + vu[k8]);
-            ldg_stream_v4_if(v[k][k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
-                             d.values != nullptr && vtk[k8] < d.positions);
+        load_tile(v[0], sw[0], i0);
+        if (i0 + 1 < n) {
+          if (!both) {
+            ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
           }
-#pragma unroll
-          for (int h = 0; h < kHalves; ++h) {
-            const SubBlockSrc ds = get_src(dring + su[h]);
-            sw[k][h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
-            ldg_stream_u32_if(sw[k][h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
-                              ds.values != nullptr && stk[h] < ds.positions);
-          }
-          __syncwarp();  // every lane has read the entries before they are handed back
-          if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
+          load_tile(v[1], sw[1], i0 + 1);
+        }
+        __syncwarp();  // every lane has read the entries before they are handed back
+        if (lane == 0) {
+          mbar_arrive(bar_desc_empty(i0 % kDescRing));
+          if (i0 + 1 < n) mbar_arrive(bar_desc_empty((i0 + 1) % kDescRing));
         }
       }
     }
