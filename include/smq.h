@@ -246,7 +246,7 @@ typedef struct smq_prefill_args {
   const uint8_t *q;               /* device [R][H][D] E4M3 */
   const float *q_scale;           /* device [R] */
   const uint16_t *weights;        /* device [R][H] bf16 */
-  const uint8_t *k_values;        /* device [total_len][D/2], 16-byte aligned */
+  const uint8_t *k_values;        /* device [total_len][D/2], 32-byte aligned */
   const uint8_t *k_scales;        /* device [total_len][D/32], 4-byte aligned */
   int64_t total_len;
   const int32_t *cu_seqlen_ks;    /* device [R] */

@@ -67,6 +67,26 @@ int encode_q(CUtensorMap* m, const uint8_t* q, int64_t qrows, int n_mma) {
   return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
 }
 
+// Key values as a 3-D tensor [pages][rows][128 FP4 values]: the copy of one
+// sub-block unpacks each 16 values (8 bytes) into a 16-byte container, with
+// the 128-byte swizzle the MMA descriptors use. The contiguous prefill
+// workspace is one page of total_len rows.
+int encode_k(CUtensorMap* m, const uint8_t* values, int64_t rows, int64_t page_stride, int64_t pages, int sbkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SMQ_ERR_CUDA;
+  if (!aligned(values, 32) || page_stride % 32 != 0 || rows > (int64_t(1) << 31) - 1 || pages > (int64_t(1) << 31) - 1)
+    return SMQ_ERR_INVALID_ARG;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(pages)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim / 2), static_cast<cuuint64_t>(page_stride)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(sbkv), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(values), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
 constexpr size_t kStatusBytes = 256;
 
 // Workspace: [status word, 256 B][per-row tile counters, max_rows int32][fp32 logits, rows x num_cols].
@@ -363,9 +383,10 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   if (rc != SMQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_k;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
   if (rc != SMQ_OK) return rc;
+  std::memset(&tm_k, 0, sizeof(tm_k));  // a paged cache is read through registers, not tensor copies
   // up to 64 candidate blocks per row the score kernel expands the rows itself
   const bool fused = !a.expansion_ready && plan->desc.candidate_topk_blocks <= smq::kMaxFusedBlocks;
   record(a.profile_events[0], s);
@@ -403,7 +424,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   sp.block_table = a.block_table;
   sp.row_indices = a.row_indices;
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
-  if (smq::launch_score(sp, true, tm_q, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (smq::launch_score(sp, true, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   if (!fuse_topk) rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);
@@ -421,13 +442,15 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
   if (!a.k_values || !a.k_scales || !a.cu_seqlen_ks || !a.cu_seqlen_ke || a.total_len <= 0 ||
       a.total_len > (int64_t(1) << 31) - 1)
     return SMQ_ERR_INVALID_ARG;
-  if (!aligned(a.k_values, 16) || !aligned(a.k_scales, 4)) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.k_values, 32) || !aligned(a.k_scales, 4)) return SMQ_ERR_INVALID_ARG;
   rc = check_device(const_cast<smq_plan*>(plan));
   if (rc != SMQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_k;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
+  if (rc != SMQ_OK) return rc;
+  rc = encode_k(&tm_k, a.k_values, a.total_len, a.total_len * (kHeadDim / 2), 1, plan->sbkv);
   if (rc != SMQ_OK) return rc;
   record(a.profile_events[0], s);
   if (!a.expansion_ready) {
@@ -441,7 +464,7 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
   sp.k_scales = a.k_scales;
   sp.total_len = a.total_len;
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
-  if (smq::launch_score(sp, false, tm_q, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (smq::launch_score(sp, false, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);

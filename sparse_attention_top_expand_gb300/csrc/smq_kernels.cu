@@ -49,9 +49,10 @@ __host__ __device__ constexpr uint32_t round_up(uint32_t x, uint32_t a) { return
 
 // One sub-block of a tile as the scheduler warp publishes it to the loaders.
 struct SubBlockSrc {
-  const uint8_t* values;  // FP4 values of its first position (64 B per position); null: not loaded
+  const uint8_t* values;  // FP4 values of its first position (64 B per position)
   const uint8_t* scales;  // UE8M0 word of its first position (4 B per position)
-  int32_t positions;      // positions that may be read (fewer at the end of a contiguous workspace)
+  int32_t row, page;      // the values' tensor-copy coordinates (row in the page, page)
+  int32_t positions;      // positions that may be read; 0: nothing is loaded
   int32_t pad;
 };
 
@@ -226,11 +227,12 @@ __device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
 // between the reader's mbarrier wait and its hand-back arrival: both are
 // compiler memory barriers, so no read moves out of that window, and the
 // compiler is free to merge and schedule the reads inside it.
-__device__ __forceinline__ void put_src(SubBlockSrc* e, const uint8_t* values, const uint8_t* scales, int positions) {
+__device__ __forceinline__ void put_src(SubBlockSrc* e, const uint8_t* values, const uint8_t* scales, int row, int page,
+                                        int positions) {
   const uint32_t a = smem_addr(e);
-  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a), "l"(values) : "memory");
-  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a + 8), "l"(scales) : "memory");
-  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(a + 16), "r"(positions) : "memory");
+  asm volatile("st.volatile.shared.v2.u64 [%0], {%1, %2};" ::"r"(a), "l"(values), "l"(scales) : "memory");
+  asm volatile("st.volatile.shared.v2.s32 [%0], {%1, %2};" ::"r"(a + 16), "r"(row), "r"(page) : "memory");
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(a + 24), "r"(positions) : "memory");
 }
 
 __device__ __forceinline__ SubBlockSrc get_src(const SubBlockSrc* e) {
@@ -578,7 +580,8 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
 
 template <bool kPaged, int kN, bool kFused>
 __global__ void __launch_bounds__(kScoreThreads, 1)
-    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q) {
+    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_k) {
   extern __shared__ uint8_t score_smem_raw[];
   uint8_t* smem = align1024(score_smem_raw);
   const ScoreLayout lay(kN, p.heads, p.rows);
@@ -611,7 +614,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // ---- prologue: barriers, per-row tile counts and their prefix ---------
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full(s), kLoaderThreads / 32);  // one arrival per loader warp
+      // one arrival per loader warp, and (tensor-copy path) the value copies' expect
+      mbar_init(bar_full(s), kLoaderThreads / 32 + (kPaged ? 0 : 1));
       mbar_init(bar_empty(s), 1);
     }
     for (int d = 0; d < kDescRing; ++d) {
@@ -634,6 +638,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     mbar_init_fence();
   }
   if (tid == 32 * kQueryWarp) prefetch_tmap(&tm_q);
+  if (!kPaged && tid == 32 * 6) prefetch_tmap(&tm_k);
   // with programmatic dependent launch the prologue above overlaps the
   // previous kernel; everything below reads what earlier kernels wrote
   griddep_launch_dependents();
@@ -743,7 +748,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int64_t t = tb + lane / spt;
         const int sub = lane % spt;
         const int col_sub = static_cast<int>(t - row0) * spt + sub;
-        int ntok = 0;
+        int ntok = 0, trow = 0, tpage = 0;
         const uint8_t* vsrc = nullptr;
         const uint8_t* ssrc = nullptr;
         if (t < tz && col_sub * sbkv < e) {  // columns below end are valid sub-blocks
@@ -758,6 +763,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
               vsrc = base + tok * (kHeadDim / 2);
               ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+              trow = static_cast<int>(tok);
+              tpage = pg;
               ntok = sbkv;
               valid = true;
             }
@@ -773,7 +780,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
           ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, ntok);
+          if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_desc_full(dslot));
           ++it;
@@ -797,7 +804,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int64_t tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
       const int64_t t = tb + lane / spt;
       const int sub = lane % spt;
-      int ntok = 0;
+      int ntok = 0, trow = 0, tpage = 0;
       const uint8_t* vsrc = nullptr;
       const uint8_t* ssrc = nullptr;
       if (t < t_end) {
@@ -824,6 +831,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                   const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
                   vsrc = base + tok * (kHeadDim / 2);
                   ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+                  trow = static_cast<int>(tok);
+                  tpage = pg;
                   ntok = sbkv;
                   valid = true;
                 }
@@ -833,6 +842,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               if (pos >= 0 && pos < p.total_len) {
                 vsrc = p.k_values + pos * (kHeadDim / 2);
                 ssrc = p.k_scales + pos * kScaleWordBytes;
+                trow = static_cast<int>(pos);  // the contiguous workspace is one page of total_len rows
                 ntok = static_cast<int>(p.total_len - pos < sbkv ? p.total_len - pos : sbkv);
                 valid = true;
               }
@@ -853,7 +863,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the lanes that resolved this tile's sub-blocks publish them
-        if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, ntok);
+        if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_desc_full(dslot));
         ++it;
@@ -1084,125 +1094,212 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   } else if (warp >= 6 && warp < 10) {
     // ======================= loaders (warps 6..9) =======================
-    // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
-    // t / 4 + 32 k (k = 0..7), so that each warp load reads 512 contiguous
-    // bytes (8 rows of one sub-block). Scale words: thread t owns key rows t
-    // and t + 128. Both are loaded kLoadAhead stages before they are needed.
-    // The values are stored into the 16-byte containers the MMA reads (8 data
-    // bytes per 16 elements, 128-byte swizzle); the scale words go to the
-    // stage half's scale block.
-    constexpr int kChunks = kTileM / 32;
-    const int q4 = warp & 3;
-    const int m = 32 * q4 + lane;
-    const uint32_t sf_base = smem_addr(smem + lay.sf);
-    const int vch = m & 3;
-    int vu[kChunks], vtk[kChunks];
-#pragma unroll
-    for (int k8 = 0; k8 < kChunks; ++k8) {
-      const int pos = (m >> 2) + 32 * k8;
-      vu[k8] = pos / sbkv;
-      vtk[k8] = pos % sbkv;
-    }
-    int su[kHalves], stk[kHalves];
-#pragma unroll
-    for (int h = 0; h < kHalves; ++h) {
-      su[h] = (m + h * kMmaM) / sbkv;
-      stk[h] = (m + h * kMmaM) % sbkv;
-    }
-    const uint32_t kv_base = smem_addr(smem + lay.kv);
-    uint4 v[kLoadAhead][kChunks];
-    uint32_t sw[kLoadAhead][kHalves];
-#pragma unroll
-    for (int k = 0; k < kLoadAhead; ++k) {
-#pragma unroll
-      for (int k8 = 0; k8 < kChunks; ++k8) v[k][k8] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    // Tiles go in pairs: slot k holds tile i0 + k. A wait costs a warp about
-    // as much as a tile's stores, so each pair takes one `empty` wait (stages
-    // are freed in tile order: the later one implies the earlier) and, once
-    // the ring runs ahead, one descriptor wait (published in tile order).
-    static_assert(kLoadAhead == 2, "the loader works on pairs of tiles");
-    auto store_tile = [&](const uint4 (&vv)[kChunks], const uint32_t (&ss)[kHalves], int j) {
-      const int s = j % NS;
-      const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
-#pragma unroll
-      for (int k8 = 0; k8 < kChunks; ++k8) {
-        // stored whether or not the chunk was loaded: an unloaded chunk holds
-        // an older key's bytes (finite E2M1 values, scale 1) in a position the
-        // epilogue never stores
-        const int pos = (m >> 2) + 32 * k8;
-        const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
-        const uint32_t swz = static_cast<uint32_t>(pos & 7);
-        sts_v2(dst + (((2 * vch) ^ swz) << 4), vv[k8].x, vv[k8].y);
-        sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), vv[k8].z, vv[k8].w);
-      }
-      // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
-      // half's block, which the copy to TMEM places at lane m, column base + m / 32
-#pragma unroll
-      for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
-      fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
-      __syncwarp();              // one arrival per warp
-      if (lane == 0) mbar_arrive(bar_full(s));
-    };
-    auto load_tile = [&](uint4 (&vv)[kChunks], uint32_t (&ss)[kHalves], int i) {
-      const SubBlockSrc* dring = desc + (i % kDescRing) * kMaxSubsPerTile;
-      // predicated loads: a branch per chunk costs more than the load
-#pragma unroll
-      for (int k8 = 0; k8 < kChunks; ++k8) {
-        const SubBlockSrc d = get_src(dring + vu[k8]);
-        ldg_stream_v4_if(vv[k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
-                         d.values != nullptr && vtk[k8] < d.positions);
-      }
-#pragma unroll
-      for (int h = 0; h < kHalves; ++h) {
-        const SubBlockSrc ds = get_src(dring + su[h]);
-        ss[h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
-        ldg_stream_u32_if(ss[h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
-                          ds.values != nullptr && stk[h] < ds.positions);
-      }
-    };
+    // A paged cache is read through registers (coalesced 16-byte loads two
+    // tiles ahead of the stage, then stores into the MMA's containers): with
+    // few tiles per CTA and keys in DRAM, the register slots add two tiles of
+    // buffering to the stages. The contiguous prefill workspace, read many
+    // times from L2, goes through tensor copies that unpack into the
+    // containers themselves.
     bool ok = true;
-    for (int i0 = 0; i0 < n + 2; i0 += 2) {
-      const int j0 = i0 - 2;  // the pair whose data sits in the slots
-      if (j0 >= 0 && j0 < n) {
-        const int jl = j0 + 1 < n ? j0 + 1 : j0;
-        // the stages are free once the MMAs of tiles j0 - NS and jl - NS have finished
-        ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        store_tile(v[0], sw[0], j0);
-        if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
+    if constexpr (kPaged) {
+      // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
+      // t / 4 + 32 k (k = 0..7), so that each warp load reads 512 contiguous
+      // bytes (8 rows of one sub-block). Scale words: thread t owns key rows t
+      // and t + 128. Both are loaded kLoadAhead stages before they are needed.
+      // The values are stored into the 16-byte containers the MMA reads (8 data
+      // bytes per 16 elements, 128-byte swizzle); the scale words go to the
+      // stage half's scale block.
+      constexpr int kChunks = kTileM / 32;
+      const int q4 = warp & 3;
+      const int m = 32 * q4 + lane;
+      const uint32_t sf_base = smem_addr(smem + lay.sf);
+      const int vch = m & 3;
+      int vu[kChunks], vtk[kChunks];
+  #pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) {
+        const int pos = (m >> 2) + 32 * k8;
+        vu[k8] = pos / sbkv;
+        vtk[k8] = pos % sbkv;
       }
-      if (i0 < n) {
-        // when the pair's second tile is already published (the ring runs ahead),
-        // nothing is waited for; otherwise each tile is waited for, so that the
-        // first loads leave as soon as their tile is published
-        const int il = i0 + 1 < n ? i0 + 1 : i0;
-        bool both = false;
-        if (lane == 0) both = mbar_test_wait(bar_desc_full(il % kDescRing), (il / kDescRing) & 1);
-        both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
-        __syncwarp();  // orders the other lanes after lane 0's acquire
-        if (!both) {
-          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
-          if (!ok) break;
+      int su[kHalves], stk[kHalves];
+  #pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        su[h] = (m + h * kMmaM) / sbkv;
+        stk[h] = (m + h * kMmaM) % sbkv;
+      }
+      const uint32_t kv_base = smem_addr(smem + lay.kv);
+      uint4 v[kLoadAhead][kChunks];
+      uint32_t sw[kLoadAhead][kHalves];
+  #pragma unroll
+      for (int k = 0; k < kLoadAhead; ++k) {
+  #pragma unroll
+        for (int k8 = 0; k8 < kChunks; ++k8) v[k][k8] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // Tiles go in pairs: slot k holds tile i0 + k. A wait costs a warp about
+      // as much as a tile's stores, so each pair takes one `empty` wait (stages
+      // are freed in tile order: the later one implies the earlier) and, once
+      // the ring runs ahead, one descriptor wait (published in tile order).
+      static_assert(kLoadAhead == 2, "the loader works on pairs of tiles");
+      auto store_tile = [&](const uint4 (&vv)[kChunks], const uint32_t (&ss)[kHalves], int j) {
+        const int s = j % NS;
+        const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
+  #pragma unroll
+        for (int k8 = 0; k8 < kChunks; ++k8) {
+          // stored whether or not the chunk was loaded: an unloaded chunk holds
+          // an older key's bytes (finite E2M1 values, scale 1) in a position the
+          // epilogue never stores
+          const int pos = (m >> 2) + 32 * k8;
+          const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
+          const uint32_t swz = static_cast<uint32_t>(pos & 7);
+          sts_v2(dst + (((2 * vch) ^ swz) << 4), vv[k8].x, vv[k8].y);
+          sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), vv[k8].z, vv[k8].w);
         }
-        load_tile(v[0], sw[0], i0);
-        if (i0 + 1 < n) {
+        // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
+        // half's block, which the copy to TMEM places at lane m, column base + m / 32
+  #pragma unroll
+        for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
+        fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
+        __syncwarp();              // one arrival per warp
+        if (lane == 0) mbar_arrive(bar_full(s));
+      };
+      auto load_tile = [&](uint4 (&vv)[kChunks], uint32_t (&ss)[kHalves], int i) {
+        const SubBlockSrc* dring = desc + (i % kDescRing) * kMaxSubsPerTile;
+        // predicated loads: a branch per chunk costs more than the load
+  #pragma unroll
+        for (int k8 = 0; k8 < kChunks; ++k8) {
+          const SubBlockSrc d = get_src(dring + vu[k8]);
+          ldg_stream_v4_if(vv[k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
+                           d.values != nullptr && vtk[k8] < d.positions);
+        }
+  #pragma unroll
+        for (int h = 0; h < kHalves; ++h) {
+          const SubBlockSrc ds = get_src(dring + su[h]);
+          ss[h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
+          ldg_stream_u32_if(ss[h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
+                            ds.values != nullptr && stk[h] < ds.positions);
+        }
+      };
+      for (int i0 = 0; i0 < n + 2; i0 += 2) {
+        const int j0 = i0 - 2;  // the pair whose data sits in the slots
+        if (j0 >= 0 && j0 < n) {
+          const int jl = j0 + 1 < n ? j0 + 1 : j0;
+          // the stages are free once the MMAs of tiles j0 - NS and jl - NS have finished
+          ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+          store_tile(v[0], sw[0], j0);
+          if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
+        }
+        if (i0 < n) {
+          // when the pair's second tile is already published (the ring runs ahead),
+          // nothing is waited for; otherwise each tile is waited for, so that the
+          // first loads leave as soon as their tile is published
+          const int il = i0 + 1 < n ? i0 + 1 : i0;
+          bool both = false;
+          if (lane == 0) both = mbar_test_wait(bar_desc_full(il % kDescRing), (il / kDescRing) & 1);
+          both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
+          __syncwarp();  // orders the other lanes after lane 0's acquire
           if (!both) {
-            ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
           }
-          load_tile(v[1], sw[1], i0 + 1);
+          load_tile(v[0], sw[0], i0);
+          if (i0 + 1 < n) {
+            if (!both) {
+              ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+              if (!ok) break;
+            }
+            load_tile(v[1], sw[1], i0 + 1);
+          }
+          __syncwarp();  // every lane has read the entries before they are handed back
+          if (lane == 0) {
+            mbar_arrive(bar_desc_empty(i0 % kDescRing));
+            if (i0 + 1 < n) mbar_arrive(bar_desc_empty((i0 + 1) % kDescRing));
+          }
         }
-        __syncwarp();  // every lane has read the entries before they are handed back
-        if (lane == 0) {
-          mbar_arrive(bar_desc_empty(i0 % kDescRing));
-          if (i0 + 1 < n) mbar_arrive(bar_desc_empty((i0 + 1) % kDescRing));
+      }
+    } else {
+      // Key values: tensor copies issued by warp 6, one per sub-block (lane l
+      // copies sub-block l). The copy unpacks each 16 FP4 values (8 bytes) into
+      // the 16-byte container the MMA reads (16U4_ALIGN16B) with the 128-byte
+      // swizzle, and completes on the stage's `full` barrier.
+      // Scale words: thread t owns key rows t and t + 128; it loads them into
+      // registers two tiles ahead and stores them into the stage half's scale
+      // block once the stage is free.
+      // Step i: store the scale words of tile i - 2 (the slot is reloaded next);
+      // read tile i's descriptors and load its scale words; wait for its stage
+      // and issue its value copies.
+      const int q4 = warp & 3;
+      const int m = 32 * q4 + lane;
+      const uint32_t sf_base = smem_addr(smem + lay.sf);
+      const uint32_t kv_base = smem_addr(smem + lay.kv);
+      const bool copier = warp == 6 && lane < spt;
+      const uint32_t sub_bytes = static_cast<uint32_t>(sbkv) * kRowBytes;  // one sub-block in the stage
+      // the copy's transaction count is the packed source size (half its footprint in the stage)
+      const uint32_t sub_tx = static_cast<uint32_t>(sbkv) * (kHeadDim / 2);
+      int su[kHalves], stk[kHalves];
+  #pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        su[h] = (m + h * kMmaM) / sbkv;
+        stk[h] = (m + h * kMmaM) % sbkv;
+      }
+      uint32_t sw[2][kHalves];
+      for (int i0 = 0; i0 < n + 2 && ok; i0 += 2) {
+  #pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int i = i0 + k;
+          const int j = i - 2;  // its scale words sit in slot k: store them before slot k is reloaded
+          if (j >= 0 && j < n) {
+            // scale word of key row m of each half: word 4 (m % 32) + m / 32 of the
+            // half's block, which the copy to TMEM places at lane m, column base + m / 32
+            const int s = j % NS;
+  #pragma unroll
+            for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, sw[k][h]);
+            fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
+            __syncwarp();              // one arrival per warp
+            if (lane == 0) mbar_arrive(bar_full(s));
+          }
+          if (i < n) {
+            const int dslot = i % kDescRing;
+            ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+            const SubBlockSrc* dring = desc + dslot * kMaxSubsPerTile;
+  #pragma unroll
+            for (int h = 0; h < kHalves; ++h) {
+              const SubBlockSrc ds = get_src(dring + su[h]);
+              sw[k][h] = 0x7F7F7F7Fu;  // scale 1 where no key is loaded
+              ldg_stream_u32_if(sw[k][h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
+                                stk[h] < ds.positions);
+            }
+            SubBlockSrc dv;
+            dv.positions = 0;
+            if (copier) dv = get_src(dring + lane);
+            __syncwarp();  // every lane has read the entries before they are handed back
+            if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
+            // the stage is free once the MMAs of tile i - NS have finished
+            const int s = i % NS;
+            ok = warp_wait(bar_empty(s), ((i / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+            if (warp == 6) {
+              const bool live = copier && dv.positions > 0;
+              const uint32_t nlive = __popc(__ballot_sync(kFullMask, live));
+              if (lane == 0) mbar_arrive_expect_tx(bar_full(s), nlive * sub_tx);
+              if (live) tma_load_3d(kv_base + s * (kTileM * kRowBytes) + lane * sub_bytes, &tm_k, 0, dv.row, dv.page,
+                                    bar_full(s));
+            }
+          }
         }
       }
     }
     if (!ok) {
       set_status(p.status, kStatusTimeout);
       *abort_flag = 1;
+    }
+    if (!kPaged && warp == 6 && *abort_flag != 0) {
+      // value copies already issued land within microseconds; let them finish
+      // before the CTA (and its shared memory) can go away
+      const uint64_t t0 = global_ns();
+      while (global_ns() - t0 < 20000u) {
+      }
     }
   }
 
@@ -1213,6 +1310,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // ---- top-k of the rows this CTA completed (their logits are in L2) ----
   if constexpr (kFused) {
     if (p.fused_topk && *abort_flag == 0) {
+      fence_proxy_async_smem();      // the tensor copies wrote these bytes; plain accesses follow
       uint8_t* scr = smem + lay.kv;  // the key stages are free now
       TopkScratch sm;
       sm.hist = reinterpret_cast<uint32_t*>(scr);
@@ -1377,9 +1475,9 @@ cudaError_t launch_pdl(void (*kernel)(P), unsigned grid, unsigned block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, params);
 }
 
-template <typename P, typename Q>
-cudaError_t launch_pdl2(void (*kernel)(P, Q), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
-                        const P& a, const Q& b) {
+template <typename... A>
+cudaError_t launch_pdl_n(void (*kernel)(A...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                         const A&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
@@ -1390,7 +1488,7 @@ cudaError_t launch_pdl2(void (*kernel)(P, Q), unsigned grid, unsigned block, siz
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a, b);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
@@ -1399,17 +1497,17 @@ cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
   return launch_pdl(expand_kernel, grid, kExpandWarps * 32, smem, stream, p);
 }
 
-cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
-                         cudaStream_t stream) {
+cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
+                         size_t smem, cudaStream_t stream) {
   const bool stat = paged && p.fused;
   if (p.n_mma == 64) {
-    if (stat) return launch_pdl2(score_kernel<true, 64, true>, grid, kScoreThreads, smem, stream, p, tm_q);
-    if (paged) return launch_pdl2(score_kernel<true, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q);
-    return launch_pdl2(score_kernel<false, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q);
+    if (stat) return launch_pdl_n(score_kernel<true, 64, true>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
+    if (paged) return launch_pdl_n(score_kernel<true, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
+    return launch_pdl_n(score_kernel<false, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
   }
-  if (stat) return launch_pdl2(score_kernel<true, 128, true>, grid, kScoreThreads, smem, stream, p, tm_q);
-  if (paged) return launch_pdl2(score_kernel<true, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q);
-  return launch_pdl2(score_kernel<false, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q);
+  if (stat) return launch_pdl_n(score_kernel<true, 128, true>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
+  if (paged) return launch_pdl_n(score_kernel<true, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
+  return launch_pdl_n(score_kernel<false, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {

@@ -22,8 +22,8 @@ constexpr int kQueryWarp = 10;
 constexpr int kMmaWarp1 = 11;       // second MMA issuer (odd tiles); warp 1 issues the even tiles
 constexpr int kEpilogueThreads = 128;
 constexpr int kLoaderThreads = 128;
+constexpr int kLoadAhead = 2;       // tiles each register-path loader thread keeps in flight
 constexpr int kScoreStages = 4;     // key stages resident in shared memory (32 KB each)
-constexpr int kLoadAhead = 2;       // stages each loader thread keeps in flight in registers
 constexpr int kMaxAccBuffers = 3;
 constexpr int kDescRing = 16;       // tiles whose source addresses may be published ahead of the loaders
 constexpr int kMaxFusedBlocks = 64; // candidate blocks per row the score kernel expands itself
@@ -150,8 +150,8 @@ struct GatherParams {
 size_t score_smem_bytes(int n_mma, int heads, int rows);
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
-cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, int grid, size_t smem,
-                         cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
+cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
+                         size_t smem, cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
