@@ -169,6 +169,20 @@ def test_ties_any_k_subset():
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
 
 
+def test_two_values_many_ties():
+    """Keys of two values only: the logits take a few distinct values, each
+    shared by many columns, so the top-k threshold falls inside a crowded bin
+    (ties ranked by column, or the radix passes when the bin overflows)."""
+    inp = synth.decode_batch(rows=8)
+    half = inp.geom.page_size * 64
+    inp.k_cache[:, :half] = 0x22  # every element 1.0
+    inp.k_cache[::3, :half] = 0x44  # every third page 3.0
+    inp.k_cache[:, half:] = 127
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, rows=range(8), mode="sparse"))
+
+
 def test_zero_rows_is_a_no_op():
     inp = synth.tiny_decode(0)
     plan = tensors.plan_for(inp.geom, max_rows=4)
