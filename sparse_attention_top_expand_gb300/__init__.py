@@ -233,10 +233,8 @@ def sparse_mqa_candidate_expand(plan: Plan, candidate_blocks, row_ks, row_ke, sp
         "sparse_mqa_candidate_expand")
 
 
-def sparse_mqa_logits_topk_decode(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke,
-                                  candidate_blocks, topk_out, sparse_indices, end, workspace,
-                                  expansion_ready: bool = False, col_indices=None, logits_out=None,
-                                  stream=None, profile_events=None) -> None:
+def _decode_args(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
+                 topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out):
     dev = plan.device
     a = SMQDecodeArgs()
     a.struct_size = ctypes.sizeof(SMQDecodeArgs)
@@ -261,9 +259,43 @@ def sparse_mqa_logits_topk_decode(plan: Plan, q, q_scale, weights, k_cache, bloc
     a.logits_out = _ptr(logits_out, _F32, "logits_out", dev)
     a.workspace = _ptr(workspace, _U8, "workspace", dev)
     a.workspace_bytes = workspace.numel()
+    return a
+
+
+def sparse_mqa_logits_topk_decode(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke,
+                                  candidate_blocks, topk_out, sparse_indices, end, workspace,
+                                  expansion_ready: bool = False, col_indices=None, logits_out=None,
+                                  stream=None, profile_events=None) -> None:
+    a = _decode_args(plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
+                     topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out)
     _set_events(a, profile_events)
     _check(load_library().sparse_mqa_logits_topk_decode(plan.handle, ctypes.byref(a), _stream(stream)),
            "sparse_mqa_logits_topk_decode")
+
+
+class DecodeCall:
+    """sparse_mqa_logits_topk_decode with its arguments marshalled once, for a
+    loop that calls it again and again on the same buffers (their contents may
+    change between calls, their addresses and shapes may not). Each call goes
+    through the same C entry point."""
+
+    def __init__(self, plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
+                 topk_out, sparse_indices, end, workspace, expansion_ready: bool = False, col_indices=None,
+                 logits_out=None):
+        self.plan = plan
+        self.args = _decode_args(plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke,
+                                 candidate_blocks, topk_out, sparse_indices, end, workspace, expansion_ready,
+                                 col_indices, logits_out)
+        # the buffers stay alive as long as the call
+        self._keep = (q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks, topk_out,
+                      sparse_indices, end, workspace, col_indices, logits_out)
+        self._fn = load_library().sparse_mqa_logits_topk_decode
+        self._ref = ctypes.byref(self.args)
+
+    def __call__(self, stream=None) -> None:
+        rc = self._fn(self.plan.handle, self._ref, _stream(stream))
+        if rc != 0:
+            _check(rc, "sparse_mqa_logits_topk_decode")
 
 
 def sparse_mqa_logits_topk_decode_noalloc(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices,
