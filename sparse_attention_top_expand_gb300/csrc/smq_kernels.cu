@@ -269,9 +269,8 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 // Candidate expansion of row r by one warp, for at most 64 candidate blocks
 // (the same result as expand_kernel): a block is kept if it lies in [0, L)
 // and no earlier candidate has the same id; the kept blocks are sorted into
-// sorted[0 .. nkept). Returns the row's column count. When `owner` is set
-// the row's sparse_indices and end are written to global memory.
-__device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_t* sorted, bool owner, int lane) {
+// sorted[0 .. *nkept_out). Returns the row's column count.
+__device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_t* sorted, int* nkept_out, int lane) {
   const int ncb = p.ncb;
   const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * ncb;
   const int c0 = lane < ncb ? cb[lane] : -1;
@@ -324,21 +323,28 @@ __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_
   }
   for (int o = 16; o > 0; o >>= 1) cols += __shfl_xor_sync(kFullMask, cols, o);
   __syncwarp();
-  if (owner) {
-    int32_t* si = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
-    for (int slot = lane; slot < p.nsb; slot += 32) {
-      const int k = slot / spb;
-      int v = -1;
-      if (k < nkept) {
-        const int sub = sorted[k] * spb + slot % spb;
-        if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
-      }
-      si[slot] = v;
-    }
-    if (lane == 0) p.end_out[r] = static_cast<int32_t>(cols);
-    __threadfence();  // visible to the CTA that selects this row's top-k
-  }
+  *nkept_out = nkept;
   return static_cast<int>(cols);
+}
+
+// The expansion of row r (sorted[0 .. nkept), `cols` columns below L) to
+// global memory: sparse_indices and end. The fence makes them visible to the
+// CTA that selects the row's top-k.
+__device__ void write_row_expansion(const ScoreParams& p, int r, int64_t L, const int32_t* sorted, int nkept,
+                                    int cols, int lane) {
+  const int sbkv = p.sbkv, spb = p.cbs / p.sbkv;
+  int32_t* si = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
+  for (int slot = lane; slot < p.nsb; slot += 32) {
+    const int k = slot / spb;
+    int v = -1;
+    if (k < nkept) {
+      const int sub = sorted[k] * spb + slot % spb;
+      if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
+    }
+    si[slot] = v;
+  }
+  if (lane == 0) p.end_out[r] = cols;
+  __threadfence();
 }
 
 // ---------------------------------------------------------------------------
@@ -737,8 +743,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (rz == row0) continue;  // no tiles (written by CTA 0)
       const int brow = p.row_indices ? p.row_indices[r] : r;
       const int ke = p.row_ke[r];
-      int e = expand_row_in_warp(p, r, ke > 0 ? ke : 0, sorted, row0 >= t_begin, lane);
-      e = e < 0 ? 0 : (e > S ? S : e);
+      int nkept = 0;
+      const int cols = expand_row_in_warp(p, r, ke > 0 ? ke : 0, sorted, &nkept, lane);
+      // the CTA with the row's first tile writes its expansion, after the first
+      // block-table loads are out so that the fence overlaps them
+      bool pending_owner = row0 >= t_begin;
+      int e = cols < 0 ? 0 : (cols > S ? S : cols);
       // read by the epilogue once it sees this row's first accumulator
       if (lane == 0) st_volatile_s32(rend + (r - r_first), e);
       __syncwarp();
@@ -751,25 +761,32 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         int ntok = 0, trow = 0, tpage = 0;
         const uint8_t* vsrc = nullptr;
         const uint8_t* ssrc = nullptr;
-        if (t < tz && col_sub * sbkv < e) {  // columns below end are valid sub-blocks
+        const bool want = t < tz && col_sub * sbkv < e;  // columns below end are valid sub-blocks
+        int64_t tpos = 0;
+        int pg = -1;
+        if (want) {
           const int sb = sorted[col_sub / spb] * spb + col_sub % spb;
-          const int64_t tpos = static_cast<int64_t>(sb) * sbkv;
+          tpos = static_cast<int64_t>(sb) * sbkv;
           const int64_t slot = tpos / p.page_size;
-          bool valid = false;
-          if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride) {
-            const int pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
-            if (pg >= 0 && pg < p.num_pages) {
-              const int64_t tok = tpos % p.page_size;
-              const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
-              vsrc = base + tok * (kHeadDim / 2);
-              ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
-              trow = static_cast<int>(tok);
-              tpage = pg;
-              ntok = sbkv;
-              valid = true;
-            }
+          if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
+            pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
+        }
+        if (pending_owner) {
+          write_row_expansion(p, r, ke > 0 ? ke : 0, sorted, nkept, cols, lane);
+          pending_owner = false;
+        }
+        if (want) {
+          if (pg >= 0 && pg < p.num_pages) {
+            const int64_t tok = tpos % p.page_size;
+            const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
+            vsrc = base + tok * (kHeadDim / 2);
+            ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+            trow = static_cast<int>(tok);
+            tpage = pg;
+            ntok = sbkv;
+          } else {
+            set_status(p.status, kStatusBounds);
           }
-          if (!valid) set_status(p.status, kStatusBounds);
         }
         for (int k = 0; k < tiles_per_batch; ++k) {
           if (tb + k >= tz) break;

@@ -218,6 +218,36 @@ def test_repeat_calls_are_deterministic():
     assert torch.equal(first[0], dev.topk_out) and torch.equal(first[1], dev.logits)
 
 
+def test_prepared_call_matches_the_plain_call():
+    """DecodeCall marshals the arguments once; each call must give the plain
+    call's bytes, also after the inputs are rewritten in place."""
+    inp = synth.decode_batch(rows=16)
+    plan, dev, status = run_decode(inp)
+    _ok(status)
+    ref = (dev.topk_out.clone(), dev.logits.clone())
+    call = smq.DecodeCall(plan, dev.q, dev.q_scale, dev.weights, dev.k_cache, dev.block_table, dev.row_indices,
+                          dev.row_ke, dev.candidate_blocks, dev.topk_out, dev.sparse_indices, dev.end, dev.workspace,
+                          col_indices=dev.col_indices, logits_out=dev.logits)
+    dev.topk_out.fill_(-7)
+    call()
+    _ok(smq.smq_get_status(dev.workspace))
+    assert torch.equal(dev.topk_out, ref[0]) and torch.equal(dev.logits, ref[1])
+    # new queries and weights written into the same buffers
+    import copy
+    fresh = synth.decode_batch(seed=9, rows=16)
+    other = copy.copy(inp)
+    other.q, other.q_scale, other.weights = fresh.q, fresh.q_scale, fresh.weights
+    other_dev = tensors.DecodeDevice(other, plan)
+    for name in ("q", "q_scale", "weights"):
+        getattr(dev, name).copy_(getattr(other_dev, name))
+    call()
+    _ok(smq.smq_get_status(dev.workspace))
+    other_dev.run(plan)
+    _ok(smq.smq_get_status(other_dev.workspace))
+    assert not torch.equal(dev.topk_out, ref[0])
+    assert torch.equal(dev.topk_out, other_dev.topk_out) and torch.equal(dev.logits, other_dev.logits)
+
+
 def test_tile_counters_are_left_at_zero():
     """Rows whose top-k the score kernel selects count finished tiles in the
     workspace; a call leaves those counters at zero for the next call."""
