@@ -1368,12 +1368,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // Top-k: radix select over order-preserving keys, one CTA per row.
 // ===========================================================================
 // One CTA per row (rows whose top-k the score kernel does not select itself).
-// Rows are many and each CTA is latency bound, so the launch bound keeps 3,
-// 2 or 1 CTAs per SM resident (at most 42, 64 or 128 registers a thread).
-template <int kJ>
-__global__ void __launch_bounds__(kTopkThreads, kJ <= 8 ? 3 : (kJ <= 16 ? 2 : 1))
+// Rows are many and each CTA is latency bound: rows of up to 4096 columns take
+// 256 threads, wider ones 512, and the launch bound keeps as many CTAs per SM
+// resident as 64 (or, 32 keys a thread, 128) registers a thread allow.
+template <int kThreads, int kJ>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? (kJ <= 8 ? 6 : 4) : (kJ <= 16 ? 2 : 1))
     topk_kernel(const __grid_constant__ TopkParams p) {
-  constexpr int kWarps = kTopkThreads / 32;
+  constexpr int kWarps = kThreads / 32;
+  static_assert(kThreads >= 256, "the 8-bit passes give each of the 256 bins a thread");
   extern __shared__ int32_t sidx[];  // [nsb] sparse sub-block ids of the row
   __shared__ __align__(16) uint32_t hist[256 * 32];
   __shared__ int bsum[256];
@@ -1385,7 +1387,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= 8 ? 3 : (kJ <= 16 ? 2 : 1)
   const int r = blockIdx.x;
   const int S = p.num_cols;
   const TopkScratch sm{hist, bsum, wsum, chunk, sidx, sel};
-  select_topk<kTopkThreads, kJ, false>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
+  select_topk<kThreads, kJ, false>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
                                 p.sparse_indices + static_cast<int64_t>(r) * p.nsb, p.nsb, p.sbkv,
                                 p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
                                 p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr,
@@ -1447,9 +1449,10 @@ cudaError_t prepare_kernels(int n_mma) {
                        reinterpret_cast<const void*>(&score_kernel<true, 128, true>),
                        reinterpret_cast<const void*>(&score_kernel<true, 128, false>),
                        reinterpret_cast<const void*>(&score_kernel<false, 128, false>),
-                       reinterpret_cast<const void*>(&topk_kernel<8>),
-                       reinterpret_cast<const void*>(&topk_kernel<16>),
-                       reinterpret_cast<const void*>(&topk_kernel<32>),
+                       reinterpret_cast<const void*>(&topk_kernel<256, 8>),
+                       reinterpret_cast<const void*>(&topk_kernel<256, 16>),
+                       reinterpret_cast<const void*>(&topk_kernel<512, 16>),
+                       reinterpret_cast<const void*>(&topk_kernel<512, 32>),
                        reinterpret_cast<const void*>(&expand_kernel),
                        reinterpret_cast<const void*>(&gather_kernel)};
   for (const void* f : all) {
@@ -1529,9 +1532,11 @@ cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.nsb) * 4;
-  if (p.num_cols <= 8 * kTopkThreads) return launch_pdl(topk_kernel<8>, p.rows, kTopkThreads, smem, stream, p);
-  if (p.num_cols <= 16 * kTopkThreads) return launch_pdl(topk_kernel<16>, p.rows, kTopkThreads, smem, stream, p);
-  return launch_pdl(topk_kernel<32>, p.rows, kTopkThreads, smem, stream, p);
+  if (p.num_cols <= 8 * 256) return launch_pdl(topk_kernel<256, 8>, p.rows, 256, smem, stream, p);
+  if (p.num_cols <= 16 * 256) return launch_pdl(topk_kernel<256, 16>, p.rows, 256, smem, stream, p);
+  if (p.num_cols <= 16 * 512) return launch_pdl(topk_kernel<512, 16>, p.rows, 512, smem, stream, p);
+  static_assert(32 * 512 >= kMaxSparseCols, "the widest top-k kernel covers every row");
+  return launch_pdl(topk_kernel<512, 32>, p.rows, 512, smem, stream, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {

@@ -43,7 +43,6 @@ static_assert(kScoreStages < 2 * acc_buffers(64), "accumulator parity waits need
 __host__ __device__ constexpr int score_tmem_columns(int n_mma) {
   return acc_buffers(n_mma) * kHalves * n_mma + 4 * kHalves * kScoreStages + 4 <= 256 ? 256 : 512;
 }
-constexpr int kTopkThreads = 512;
 constexpr int kFusedTopkCols = kScoreThreads * 22;  // widest row the score kernel selects itself
 constexpr int kExpandWarps = 8;
 constexpr int kMaxRowsPerCall = 8192;

@@ -41,6 +41,8 @@ GEOMS = [
     (72, 64, 64, 8, 128, (64, 1100)),
     (128, 64, 128, 7, 512, (1, 2500)),
     (128, 32, 64, 12, 64, (500, 1500)),
+    # more than 64 candidate blocks: expansion and top-k in their own kernels (16384 columns)
+    (64, 64, 128, 128, 2048, (14000, 20000)),
 ]
 
 
