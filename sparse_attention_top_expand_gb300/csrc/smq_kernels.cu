@@ -200,20 +200,6 @@ __device__ __forceinline__ void ldg_stream_u32_if(uint32_t& v, const void* p, bo
                : "l"(p), "r"(pred ? 1 : 0));
 }
 
-__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t a) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
