@@ -10,24 +10,28 @@
 //   gather_kernel  paged MXFP4 cache -> contiguous (values, scales) workspace
 //
 // The score kernel is a persistent, warp-specialised pipeline with one CTA
-// per SM:
-//  - warp 0 (scheduler): it resolves each 128-position tile's sub-blocks to
-//    source addresses (sparse id, block-table page, bounds) and publishes
-//    them per pipeline stage. When the row changes it TMA-loads the row's Q
+// per SM. A tile (stage) is 256 positions, two MMA halves of 128.
+//  - warp 0 (scheduler): it resolves each tile's sub-blocks to source
+//    addresses (sparse id, block-table page, bounds) and publishes them into a
+//    ring. For decode rows with at most 64 candidate blocks it first expands
+//    the row itself.
+//  - warp 10 (query loader): when the row changes it TMA-loads the row's Q
 //    tile (E4M3, 128-byte swizzle) and bf16 head weights.
-//  - warps 6..9 (loaders): they load each tile's FP4 values in 512-byte
-//    coalesced warp loads and its UE8M0 scale words six tiles ahead, then
-//    store the values into the padded 16-byte containers that
-//    kind::mxf8f6f4 reads for E2M1 (8 data bytes per 16 elements, 128-byte
-//    swizzle). Thread m writes the scale word of key row m into the stage's
-//    512-byte scale block in shared memory.
-//  - warps 1 and 11 (MMA, even and odd tiles): one thread copies the stage's
-//    scale block to TMEM (tcgen05.cp; row m of A reads lane m, column
-//    base + m/32, byte = scale id) and issues 4 x tcgen05.mma kind::mxf8f6f4
-//    with UE8M0 block scales, M = 128 positions, N = heads, K = 32 each. The
-//    fp32 accumulators live in TMEM, several in flight.
+//  - warps 6..9 (loaders): paged caches go through registers (512-byte
+//    coalesced warp loads two tiles ahead, then stores into the padded 16-byte
+//    containers that kind::mxf8f6f4 reads for E2M1: 8 data bytes per 16
+//    elements, 128-byte swizzle). The contiguous prefill workspace goes through
+//    tensor copies that unpack into those containers themselves. Thread m
+//    writes the scale words of key rows m and m + 128 into the stage's
+//    512-byte scale blocks.
+//  - warps 1 and 11 (MMA, alternate tiles): one thread copies a half's scale
+//    block to TMEM (tcgen05.cp; row m of A reads lane m, column base + m/32,
+//    byte = scale id) and issues 4 x tcgen05.mma kind::mxf8f6f4 with UE8M0
+//    block scales, M = 128 positions, N = heads, K = 32 each. The fp32
+//    accumulators live in TMEM, three in flight.
 //  - warps 2..5 (epilogue): one TMEM lane (= one position) per thread; they
-//    reduce over heads with ReLU and the weights.
+//    reduce over heads with ReLU and the weights. For narrow decode batches
+//    the CTA that completes a row then selects its top-k.
 // Every wait is bounded. A wait that gives up sets SMQ_ERR_TIMEOUT in the
 // status word and the CTA winds down. Out-of-range page / row / block ids set
 // SMQ_ERR_BOUNDS, and the load is skipped.
@@ -635,7 +639,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // previous kernel; everything below reads what earlier kernels wrote
   griddep_launch_dependents();
   griddep_wait();
-  // tiles of row r: from its end, or (rows expanded here) the bound ceil(min(row_ke, S) / 128)
+  // tiles of row r: from its end, or (rows expanded here) the bound ceil(min(row_ke, S) / 256)
   const int per = (R + kScoreThreads - 1) / kScoreThreads;
   const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
   auto tiles_of = [&](int r) {
@@ -1108,7 +1112,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
       // t / 4 + 32 k (k = 0..7), so that each warp load reads 512 contiguous
       // bytes (8 rows of one sub-block). Scale words: thread t owns key rows t
-      // and t + 128. Both are loaded kLoadAhead stages before they are needed.
+      // and t + 128. Both are loaded kLoadAhead tiles before they are needed.
       // The values are stored into the 16-byte containers the MMA reads (8 data
       // bytes per 16 elements, 128-byte swizzle); the scale words go to the
       // stage half's scale block.
