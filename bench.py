@@ -220,6 +220,8 @@ def make_inputs(workload: str, rank: int):
         return synth.long_context_decode(seed=rank_seed(4, rank))
     if workload == "prefill_chunk":
         return synth.prefill_chunk(seed=rank_seed(2, rank))
+    if workload == "prefill_chunk_paged":  # the same chunk, read in place from the paged cache
+        return synth.prefill_as_decode(synth.prefill_chunk(seed=rank_seed(2, rank)))
     if workload == "shared_schedule":
         return synth.shared_schedule_layers(seed=rank_seed(3, rank))
     raise SystemExit(f"unknown workload {workload}")
@@ -314,7 +316,8 @@ def run_ours(args, rank, world, dist):
     else:
         decode_launches = 3
     launches_per_step = {"decode_batch": decode_launches, "long_context_decode": decode_launches,
-                         "prefill_chunk": 4, "shared_schedule": 1 + 2 * len(layers)}[args.workload]
+                         "prefill_chunk": 4, "prefill_chunk_paged": decode_launches,
+                         "shared_schedule": 1 + 2 * len(layers)}[args.workload]
 
     for i in range(args.warmup):
         step(i)
@@ -400,7 +403,7 @@ def run_ours(args, rank, world, dist):
     if kernel_ms:
         g = base.geom
         nsub = sum(int(x) for x in (reps[0][0].end.cpu().numpy() + plan.sparse_block_kv - 1) // plan.sparse_block_kv)
-        if prefill:
+        if prefill or args.workload == "prefill_chunk_paged":  # a contraction-bound chunk
             flops = 2.0 * g.num_heads * g.head_dim * cols
             achieved = flops / (kernel_ms["score"] / 1e3) / 1e12
             peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
@@ -714,7 +717,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
-                    choices=["decode_batch", "long_context_decode", "prefill_chunk", "shared_schedule"])
+                    choices=["decode_batch", "long_context_decode", "prefill_chunk", "prefill_chunk_paged",
+                             "shared_schedule"])
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -347,6 +347,22 @@ def shared_schedule_layers(seed: int = 3, layers: int = 4, rows: int = 64):
     return out
 
 
+def prefill_as_decode(inp: PrefillInputs) -> DecodeInputs:
+    """The chunk's rows as paged decode rows, for in-place paged prefill (no
+    gather): row r reads its sequence's pages through the sequence's
+    block-table row, with its causal end, relative to the sequence start, as
+    its context length. Candidate blocks and output ids stay relative to the
+    sequence start. Every row's range must start at its sequence's start."""
+    ks = np.asarray(inp.cu_seqlen_ks, dtype=np.int64)
+    seq = np.searchsorted(np.asarray(inp.cu_seq_lens, dtype=np.int64), ks, side="right") - 1
+    if not np.array_equal(np.asarray(inp.cu_seq_lens)[seq], ks):
+        raise ValueError("a row's key range does not start at its sequence's start")
+    return DecodeInputs(geom=inp.geom, q=inp.q, q_scale=inp.q_scale, weights=inp.weights, k_cache=inp.k_cache,
+                        block_table=inp.seq_block_table, row_indices=seq.astype(np.int32),
+                        row_ke=(np.asarray(inp.cu_seqlen_ke, dtype=np.int64) - ks).astype(np.int32),
+                        candidate_blocks=inp.candidate_blocks)
+
+
 def prefill_chunk(seed: int = 2, seq_lens=(28672, 36864), queries_per_seq: int = 2048,
                   num_heads: int = 64, page_size: int = 64, cbs: int = 128,
                   ncb: int = 32, topk: int = 2048) -> PrefillInputs:

@@ -103,6 +103,24 @@ def test_prefill_unaligned_sequence_starts():
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
 
 
+def test_prefill_rows_through_the_paged_decode_call():
+    """In-place paged prefill: the chunk's rows, run through the paged decode
+    call on the cache itself, give the gather path's expansion, logits and ids."""
+    inp = synth.prefill_chunk(seed=12, seq_lens=(1500, 2300, 700), queries_per_seq=40, num_heads=64,
+                              page_size=64, cbs=128, ncb=6, topk=300)
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    dec = synth.prefill_as_decode(inp)
+    plan_d, ddev, status_d = run_decode(dec)
+    _ok(status_d)
+    assert torch.equal(ddev.sparse_indices, dev.sparse_indices) and torch.equal(ddev.end, dev.end)
+    valid = torch.arange(plan.num_sparse_cols, device=dev.end.device)[None, :] < dev.end[:, None].long()
+    assert torch.equal(ddev.logits[valid], dev.logits[valid])
+    assert torch.equal(ddev.topk_out, dev.topk_out)
+    check_rows(dec, ddev, plan_d, oracle.reference_rows(dec, rows=range(0, dec.rows, 7), mode="sparse"),
+               all_rows=False)
+
+
 def test_prefill_chunk_full_size():
     """4096 rows from 2 sequences (28672 + 36864), causal ranges, topk 2048."""
     inp = synth.prefill_chunk()
