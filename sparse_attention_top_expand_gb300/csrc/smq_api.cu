@@ -386,7 +386,12 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   CUtensorMap tm_q, tm_k;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
   if (rc != SMQ_OK) return rc;
-  std::memset(&tm_k, 0, sizeof(tm_k));  // a paged cache is read through registers, not tensor copies
+  // A paged cache is read through registers (coalesced loads two tiles ahead
+  // buffer DRAM latency best), unless many rows share each block-table row (a
+  // prefill chunk run in place): then the pages are re-read from L2 and
+  // unpacking tensor copies are faster. Copies need a 32-byte aligned cache.
+  std::memset(&tm_k, 0, sizeof(tm_k));
+  bool copy = a.rows >= 8 * a.bt_rows && plan->n_mma == 64 && aligned(a.k_cache, 32);
   // up to 64 candidate blocks per row the score kernel expands the rows itself
   const bool fused = !a.expansion_ready && plan->desc.candidate_topk_blocks <= smq::kMaxFusedBlocks;
   record(a.profile_events[0], s);
@@ -397,6 +402,8 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   record(a.profile_events[1], s);
   smq::ScoreParams sp = score_params(plan, c);
   sp.fused = fused ? 1 : 0;
+  copy = copy && fused &&
+         encode_k(&tm_k, a.k_cache, plan->desc.page_size, plan->page_bytes, a.num_pages, plan->sbkv) == SMQ_OK;
   // the score kernel also selects the top-k of the rows it expands when they are narrow enough
   // and few enough that the CTA finishing a row rarely has a second one to select (a wide
   // batch of rows is faster in the separate kernel, one CTA per row over every SM)
@@ -424,7 +431,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   sp.block_table = a.block_table;
   sp.row_indices = a.row_indices;
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
-  if (smq::launch_score(sp, true, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (smq::launch_score(sp, true, copy, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   if (!fuse_topk) rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);
@@ -464,7 +471,7 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
   sp.k_scales = a.k_scales;
   sp.total_len = a.total_len;
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
-  if (smq::launch_score(sp, false, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  if (smq::launch_score(sp, false, true, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);
   rc = run_topk(plan, c, sp, s);
   record(a.profile_events[3], s);

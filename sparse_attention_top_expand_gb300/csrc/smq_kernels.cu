@@ -574,7 +574,9 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   }
 }
 
-template <bool kPaged, int kN, bool kFused>
+// kCopy: key values by tensor copies (the contiguous workspace always; a paged
+// cache whose pages many rows re-read from L2) rather than through registers.
+template <bool kPaged, int kN, bool kFused, bool kCopy = !kPaged>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_k) {
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       // one arrival per loader warp, and (tensor-copy path) the value copies' expect
-      mbar_init(bar_full(s), kLoaderThreads / 32 + (kPaged ? 0 : 1));
+      mbar_init(bar_full(s), kLoaderThreads / 32 + (kCopy ? 1 : 0));
       mbar_init(bar_empty(s), 1);
     }
     for (int d = 0; d < kDescRing; ++d) {
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     mbar_init_fence();
   }
   if (tid == 32 * kQueryWarp) prefetch_tmap(&tm_q);
-  if (!kPaged && tid == 32 * 6) prefetch_tmap(&tm_k);
+  if (kCopy && tid == 32 * 6) prefetch_tmap(&tm_k);
   // with programmatic dependent launch the prologue above overlaps the
   // previous kernel; everything below reads what earlier kernels wrote
   griddep_launch_dependents();
@@ -1108,7 +1110,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // times from L2, goes through tensor copies that unpack into the
     // containers themselves.
     bool ok = true;
-    if constexpr (kPaged) {
+    if constexpr (!kCopy) {
       // Key values: loader thread t owns the 16-byte chunk t % 4 of key rows
       // t / 4 + 32 k (k = 0..7), so that each warp load reads 512 contiguous
       // bytes (8 rows of one sub-block). Scale words: thread t owns key rows t
@@ -1301,7 +1303,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       set_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    if (!kPaged && warp == 6 && *abort_flag != 0) {
+    if (kCopy && warp == 6 && *abort_flag != 0) {
       // value copies already issued land within microseconds; let them finish
       // before the CTA (and its shared memory) can go away
       const uint64_t t0 = global_ns();
@@ -1439,6 +1441,7 @@ cudaError_t prepare_kernels(int n_mma) {
                        reinterpret_cast<const void*>(&score_kernel<true, 128, true>),
                        reinterpret_cast<const void*>(&score_kernel<true, 128, false>),
                        reinterpret_cast<const void*>(&score_kernel<false, 128, false>),
+                       reinterpret_cast<const void*>(&score_kernel<true, 64, true, true>),
                        reinterpret_cast<const void*>(&topk_kernel<256, 8>),
                        reinterpret_cast<const void*>(&topk_kernel<256, 16>),
                        reinterpret_cast<const void*>(&topk_kernel<512, 16>),
@@ -1452,11 +1455,12 @@ cudaError_t prepare_kernels(int n_mma) {
   const void* score[] = {reinterpret_cast<const void*>(&score_kernel<true, 64, true>),
                          reinterpret_cast<const void*>(&score_kernel<true, 64, false>),
                          reinterpret_cast<const void*>(&score_kernel<false, 64, false>),
+                         reinterpret_cast<const void*>(&score_kernel<true, 64, true, true>),
                          reinterpret_cast<const void*>(&score_kernel<true, 128, true>),
                          reinterpret_cast<const void*>(&score_kernel<true, 128, false>),
                          reinterpret_cast<const void*>(&score_kernel<false, 128, false>)};
-  for (int i = 0; i < 6; ++i) {
-    if ((i < 3) != (n_mma == 64)) continue;
+  for (int i = 0; i < 7; ++i) {
+    if ((i < 4) != (n_mma == 64)) continue;
     err = cudaFuncSetAttribute(score[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
   }
@@ -1507,10 +1511,12 @@ cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream) {
   return launch_pdl(expand_kernel, grid, kExpandWarps * 32, smem, stream, p);
 }
 
-cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
-                         size_t smem, cudaStream_t stream) {
+cudaError_t launch_score(const ScoreParams& p, bool paged, bool copy, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                         int grid, size_t smem, cudaStream_t stream) {
   const bool stat = paged && p.fused;
   if (p.n_mma == 64) {
+    if (stat && copy)
+      return launch_pdl_n(score_kernel<true, 64, true, true>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
     if (stat) return launch_pdl_n(score_kernel<true, 64, true>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
     if (paged) return launch_pdl_n(score_kernel<true, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
     return launch_pdl_n(score_kernel<false, 64, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);

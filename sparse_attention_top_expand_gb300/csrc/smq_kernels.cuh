@@ -149,8 +149,8 @@ struct GatherParams {
 size_t score_smem_bytes(int n_mma, int heads, int rows);
 
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
-cudaError_t launch_score(const ScoreParams& p, bool paged, const CUtensorMap& tm_q, const CUtensorMap& tm_k, int grid,
-                         size_t smem, cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
+cudaError_t launch_score(const ScoreParams& p, bool paged, bool copy, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                         int grid, size_t smem, cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
