@@ -181,7 +181,8 @@ typedef struct smq_decode_args {
   const uint8_t *q;               /* device [R][H][D] E4M3 */
   const float *q_scale;           /* device [R] */
   const uint16_t *weights;        /* device [R][H] bf16 */
-  const uint8_t *k_cache;         /* device [num_pages][page_bytes], 16-byte aligned */
+  const uint8_t *k_cache;         /* device [num_pages][page_bytes], 16-byte aligned (32-byte
+                                    aligned lets rows that share pages use tensor copies) */
   int64_t num_pages;
   const int32_t *block_table;     /* device [bt_rows][bt_stride] page ids */
   int32_t bt_rows;
