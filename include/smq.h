@@ -80,7 +80,7 @@ extern "C" {
 typedef enum smq_status {
   SMQ_OK = 0,
   SMQ_ERR_INVALID_ARG = 1,         /* null or misaligned pointer, bad size */
-  SMQ_ERR_UNSUPPORTED = 2,         /* shape or device this build cannot run */
+  SMQ_ERR_UNSUPPORTED = 2,         /* shape or device this library cannot run */
   SMQ_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < smq_workspace_size() */
   SMQ_ERR_CUDA = 4,                /* a CUDA runtime or driver call failed */
   SMQ_ERR_BOUNDS = 8,              /* device: page / row / block id out of range */
@@ -121,7 +121,7 @@ typedef struct smq_plan_info {
 /* Validate the descriptor and create a plan. It reads the device's SM
  * count and does no GPU work. The plan is host memory owned by the caller
  * until smq_plan_destroy. Returns SMQ_ERR_INVALID_ARG or
- * SMQ_ERR_UNSUPPORTED for a geometry this build does not run. */
+ * SMQ_ERR_UNSUPPORTED for a geometry this library does not run. */
 SMQ_API int smq_plan_create(const smq_plan_desc *desc, smq_plan **plan);
 SMQ_API int smq_plan_destroy(smq_plan *plan);
 SMQ_API int smq_plan_get_info(const smq_plan *plan, smq_plan_info *info);
