@@ -245,7 +245,7 @@ def valid_cols(inp, plan) -> int:
             L = int(inp.row_ke[r])
         else:
             L = int(inp.cu_seqlen_ke[r]) - int(inp.cu_seqlen_ks[r])
-        blocks = sorted({int(b) for b in inp.candidate_blocks[r] if b >= 0 and b * g.candidate_block_size < L})
+        blocks = sorted({int(b) for b in inp.candidate_blocks[r] if 0 <= int(b) and int(b) * g.candidate_block_size < L})
         for b in blocks:
             total += min(g.candidate_block_size, L - b * g.candidate_block_size)
     return total

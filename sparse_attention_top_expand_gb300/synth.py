@@ -241,12 +241,54 @@ def _distinct_blocks(rng, nblk, ncb):
     return out
 
 
+_I32_MIN, _I32_MAX = -(2 ** 31), 2 ** 31 - 1
+
+
+def adversarial_blocks(rng, ncb, L, cbs, kind):
+    """Candidate rows that exercise every rule of the expansion: ids repeated
+    within the first 32 entries and between the first and second 32,
+    -1 and other negative ids, blocks at and far past the row end.
+
+    kind "mixed": a few distinct in-range ids, each repeated, among invalid
+    ones; "lone": one in-range id repeated among invalid ones; "none": no
+    in-range id at all."""
+    nblk = (L + cbs - 1) // cbs
+    invalid_pool = np.array([-1, -2, -7, -1000, _I32_MIN, nblk, nblk + 1, nblk + 5, 4 * nblk + 3,
+                             _I32_MAX], dtype=np.int64)
+    out = rng.choice(invalid_pool, size=ncb).astype(np.int64)
+    if kind == "none" or nblk == 0:
+        return out.astype(np.int32)
+    if kind == "lone":
+        b = int(rng.integers(0, nblk))
+        slots = rng.choice(ncb, size=min(ncb, 3), replace=False)
+        if ncb > 32:  # one copy in each half
+            slots[0] = int(rng.integers(0, 32))
+            slots[-1] = int(rng.integers(32, ncb))
+        out[slots] = b
+        return out.astype(np.int32)
+    nd = max(1, min(nblk, ncb // 3))
+    ids = rng.choice(nblk, size=nd, replace=False)
+    # every distinct id once in a random slot, then repeats: some inside the
+    # first 32 slots, some in the second 32 naming an id of the first
+    slots = rng.permutation(ncb)
+    out[slots[:nd]] = ids
+    nrep = min(ncb - nd, nd)
+    for j in range(nrep):
+        out[slots[nd + j]] = ids[j % nd]
+    if ncb > 32:
+        lo = [s for s in range(32) if out[s] >= 0 and out[s] < nblk]
+        if lo:
+            out[int(rng.integers(32, ncb))] = out[lo[0]]
+    return out.astype(np.int32)
+
+
 def _touched_pages(block_table, row_indices, row_ke, cand, cbs, page_size):
     pages = set()
     for r in range(cand.shape[0]):
         bt = block_table[row_indices[r]]
         L = int(row_ke[r])
         for b in cand[r]:
+            b = int(b)
             if b < 0 or b * cbs >= L:
                 continue
             for p in range(b * cbs, min((b + 1) * cbs, L), page_size):
@@ -365,10 +407,11 @@ def prefill_as_decode(inp: PrefillInputs) -> DecodeInputs:
 
 def prefill_chunk(seed: int = 2, seq_lens=(28672, 36864), queries_per_seq: int = 2048,
                   num_heads: int = 64, page_size: int = 64, cbs: int = 128,
-                  ncb: int = 32, topk: int = 2048) -> PrefillInputs:
+                  ncb: int = 32, topk: int = 2048, cand_fn=None) -> PrefillInputs:
     """Query rows are the last ``queries_per_seq`` compressed positions of each
     sequence; row t of a sequence of length L sees positions [0, L - n + t + 1)
-    (causal).  Candidate blocks: ncb distinct ids below the row's end."""
+    (causal).  Candidate blocks: ncb distinct ids below the row's end, or
+    ``cand_fn(rng, row, n)`` when given."""
     d = HEAD_DIM
     rng = _rng(seed)
     geom = Geometry(num_heads, d, page_size, cbs, ncb, topk)
@@ -394,7 +437,10 @@ def prefill_chunk(seed: int = 2, seq_lens=(28672, 36864), queries_per_seq: int =
             n = L - queries_per_seq + t + 1
             ks[r] = cu[s]
             ke[r] = cu[s] + n
-            cand[r] = _distinct_blocks(rng, (n + cbs - 1) // cbs, ncb)
+            if cand_fn is not None:
+                cand[r] = cand_fn(rng, r, n)
+            else:
+                cand[r] = _distinct_blocks(rng, (n + cbs - 1) // cbs, ncb)
             r += 1
     cache = _fill_cache(rng, num_pages, page_size, d, np.arange(num_pages))
     return PrefillInputs(geom, q, qs, w, cache, bt, cu, ks, ke, cand)
