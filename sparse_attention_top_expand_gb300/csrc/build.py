@@ -15,6 +15,7 @@ PKG = os.path.dirname(HERE)
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsmq.so")
+TRACE_LIB = os.path.join(PKG, "libsmq_trace.so")  # -DSMQ_TRACE: phase timestamps (include/smq_trace.h)
 SOURCES = ["smq_api.cu", "smq_kernels.cu"]
 HEADERS = ["smq_kernels.cuh", "smq_ptx.cuh"]
 
@@ -36,14 +37,19 @@ def _stale(out: str) -> bool:
     if not os.path.exists(out):
         return True
     t = os.path.getmtime(out)
-    deps = [os.path.join(HERE, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "smq.h")]
+    deps = [os.path.join(HERE, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, h)
+                                                                for h in ("smq.h", "smq_trace.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _stale(LIB):
-        return LIB
-    objdir = os.path.join(PKG, "_build")
+def build(force: bool = False, verbose: bool = False, extra_flags=(), trace: bool = False) -> str:
+    """Compile libsmq.so, or with trace=True the tracing build libsmq_trace.so."""
+    out = TRACE_LIB if trace else LIB
+    if not force and not _stale(out):
+        return out
+    if trace:
+        extra_flags = (*extra_flags, "-DSMQ_TRACE")
+    objdir = os.path.join(PKG, "_build", "trace" if trace else "lib")
     os.makedirs(objdir, exist_ok=True)
     procs = []
     objs = []
@@ -55,17 +61,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)
     for cmd, p in procs:
-        out, _ = p.communicate()
+        log, _ = p.communicate()
         if verbose or p.returncode != 0:
-            sys.stdout.write(out)
+            sys.stdout.write(log)
         if p.returncode != 0:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     link = [_nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp]
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -2,6 +2,7 @@
 // plan, TMA tensor-map encoding and kernel launches. Nothing here allocates
 // device memory; every tensor is the caller's.
 #include "smq.h"
+#include "smq_trace.h"
 #include "smq_kernels.cuh"
 
 #include <cuda.h>
@@ -213,6 +214,18 @@ int run_topk(const smq_plan* p, const CommonRows& a, const smq::ScoreParams& s, 
   return smq::launch_topk(t, stream) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
 }
 
+// CTAs per row of the row-cluster kernel for a decode call of `rows` rows, or
+// 0 where it does not apply: more rows than SMs, rows wider than its limit, or
+// shared memory that does not fit.
+int row_cluster_size(const smq_plan* p, int rows) {
+  if (rows <= 0 || rows > p->num_sms || p->num_cols > smq::kRowClusterMaxCols) return 0;
+  if (smq::row_cluster_smem_bytes(p->n_mma, p->desc.num_heads, p->nsb, p->num_cols) > 232448) return 0;
+  int c = p->num_sms / rows;
+  if (c > smq::kRowClusterMaxCtas) c = smq::kRowClusterMaxCtas;
+  const int tiles = (p->num_cols + kTileM - 1) / kTileM;
+  return c > tiles ? tiles : c;  // a CTA without a tile would only wait
+}
+
 int score_grid(const smq_plan* p, int rows) {
   const int64_t max_tiles = static_cast<int64_t>(rows) * ((p->num_cols + kTileM - 1) / kTileM);
   return static_cast<int>(max_tiles < p->num_sms ? max_tiles : p->num_sms);
@@ -394,6 +407,44 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
   bool copy = a.rows >= 8 * a.bt_rows && plan->n_mma == 64 && aligned(a.k_cache, 32);
   // up to 64 candidate blocks per row the score kernel expands the rows itself
   const bool fused = !a.expansion_ready && plan->desc.candidate_topk_blocks <= smq::kMaxFusedBlocks;
+  // A narrow batch (no more rows than SMs) takes one cluster of CTAs per row,
+  // which keeps the row's logits and top-k on chip.
+  const int cluster = row_cluster_size(plan, a.rows);
+  if (cluster > 0 && !copy) {
+    const size_t smem = smq::row_cluster_smem_bytes(plan->n_mma, plan->desc.num_heads, plan->nsb, plan->num_cols);
+    record(a.profile_events[0], s);
+    if (!a.expansion_ready && !fused) {
+      rc = run_expand(plan, a.candidate_blocks, nullptr, a.row_ke, a.rows, a.sparse_indices, a.end, s);
+      if (rc != SMQ_OK) return rc;
+    }
+    record(a.profile_events[1], s);
+    smq::ScoreParams sp = score_params(plan, c);
+    sp.fused = fused ? 1 : 0;
+    sp.cluster = cluster;
+    sp.logits_out = a.logits_out;
+    sp.topk = plan->desc.topk;
+    sp.topk_ld = a.topk_ld;
+    sp.topk_out = a.topk_out;
+    sp.col_indices = a.col_indices;
+    sp.ncb = plan->desc.candidate_topk_blocks;
+    sp.cbs = plan->desc.candidate_block_size;
+    sp.candidate_blocks = a.candidate_blocks;
+    sp.row_ke = a.row_ke;
+    sp.sparse_indices_out = a.sparse_indices;
+    sp.end_out = a.end;
+    sp.k_cache = a.k_cache;
+    sp.num_pages = a.num_pages;
+    sp.page_bytes = plan->page_bytes;
+    sp.page_size = plan->desc.page_size;
+    sp.bt_rows = a.bt_rows;
+    sp.bt_stride = a.bt_stride;
+    sp.block_table = a.block_table;
+    sp.row_indices = a.row_indices;
+    if (smq::launch_row_cluster(sp, tm_q, smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+    record(a.profile_events[2], s);
+    record(a.profile_events[3], s);
+    return SMQ_OK;
+  }
   record(a.profile_events[0], s);
   if (!a.expansion_ready && !fused) {
     rc = run_expand(plan, a.candidate_blocks, nullptr, a.row_ke, a.rows, a.sparse_indices, a.end, s);
@@ -530,5 +581,14 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const sm
   a.workspace_bytes = kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES;
   return sparse_mqa_logits_topk_decode(plan, &a, stream);
 }
+
+#ifdef SMQ_TRACE
+SMQ_API int smq_trace_read(uint64_t* host, size_t count) {
+  if (!host) return SMQ_ERR_INVALID_ARG;
+  return smq::trace_read(host, count) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+SMQ_API int smq_trace_clear(void) { return smq::trace_clear() == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA; }
+#endif
 
 }  // extern "C"

@@ -122,6 +122,26 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) { atomicOr
 
 }  // namespace
 
+#ifdef SMQ_TRACE
+__device__ uint64_t g_trace[kTraceCtas * kTraceSlots];
+
+__device__ __forceinline__ void trace_mark(int slot) {
+  if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceSlots + slot] = global_ns();
+}
+
+cudaError_t trace_read(uint64_t* host, size_t count) {
+  if (count > sizeof(g_trace) / sizeof(uint64_t)) count = sizeof(g_trace) / sizeof(uint64_t);
+  return cudaMemcpyFromSymbol(host, g_trace, count * sizeof(uint64_t));
+}
+
+cudaError_t trace_clear() {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_trace);
+  return e == cudaSuccess ? cudaMemset(p, 0, sizeof(g_trace)) : e;
+}
+#endif
+
+
 size_t score_smem_bytes(int n_mma, int heads, int rows) {
   return ScoreLayout(n_mma, heads, rows).total + 1024;
 }
@@ -260,11 +280,20 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 // (the same result as expand_kernel): a block is kept if it lies in [0, L)
 // and no earlier candidate has the same id; the kept blocks are sorted into
 // sorted[0 .. *nkept_out). Returns the row's column count.
+__device__ int expand_row_in_warp(const ScoreParams& p, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
+                                   int lane);
+
 __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_t* sorted, int* nkept_out, int lane) {
+  const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * p.ncb;
+  return expand_row_in_warp(p, L, lane < p.ncb ? cb[lane] : -1, lane + 32 < p.ncb ? cb[lane + 32] : -1, sorted,
+                            nkept_out, lane);
+}
+
+// The same with the row's candidates already loaded: lane l holds ids l (c0)
+// and l + 32 (c1), -1 past the row's ncb.
+__device__ int expand_row_in_warp(const ScoreParams& p, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
+                                   int lane) {
   const int ncb = p.ncb;
-  const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * ncb;
-  const int c0 = lane < ncb ? cb[lane] : -1;
-  const int c1 = lane + 32 < ncb ? cb[lane + 32] : -1;
   const uint32_t lt = (1u << lane) - 1u;
   auto in_range = [&](int b) { return b >= 0 && static_cast<int64_t>(b) * p.cbs < L; };
   // first occurrence: no lower lane (and for c1 no c0 at all) holds the same id.
@@ -377,7 +406,9 @@ struct TopkScratch {
 // the row's end is read (after the key loads are issued); sparse_row: the
 // row's sparse sub-block ids. Logits and ids may have been written by other
 // CTAs of the same kernel, so they are read from L2.
-template <int kThreads, int kJ, bool kWide>
+// kShared: L and the ids (sm.sidx, sparse_row unused) are already in this
+// CTA's shared memory.
+template <int kThreads, int kJ, bool kWide, bool kShared = false>
 __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k, const int32_t* sparse_row, int nsb,
                             int sbkv, int32_t* out, int32_t* colo, float* fill, const TopkScratch& sm) {
   constexpr int kWarps = kThreads / 32;
@@ -393,11 +424,12 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
     const int c = tid + j * kThreads;
-    raw[j] = c < S ? __ldcg(L + c) : 0.f;
+    raw[j] = c < S ? (kShared ? L[c] : __ldcg(L + c)) : 0.f;
   }
   int e = *end_src;
   e = e < 0 ? 0 : (e > S ? S : e);
-  for (int i = tid; i < nsb; i += kThreads) sm.sidx[i] = __ldcg(sparse_row + i);
+  if constexpr (!kShared)
+    for (int i = tid; i < nsb; i += kThreads) sm.sidx[i] = __ldcg(sparse_row + i);
   uint4* hist4 = reinterpret_cast<uint4*>(hist);
   for (int i = tid; i < (kWide ? kTopkBins : 256 * 32) / 4; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
   if (fill)
@@ -406,6 +438,7 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   const int sb_shift = 31 - __clz(sbkv);  // the sub-block size is a power of two (16..128)
   auto token = [&](int c) { return (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1)); };
   __syncthreads();
+  if (kShared && tid == 0) SMQ_MARK(23);
   if (e <= k) {
     for (int c = tid; c < k; c += kThreads) {
       out[c] = c < e ? token(c) : -1;
@@ -468,6 +501,7 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
     prefix = (prefix << wbits) | static_cast<uint32_t>(sel_bin[pass]);
     need -= sel_above[pass];
     done_bits += wbits;
+    if (kShared && tid == 0) SMQ_MARK(24 + pass);
     if (need == sel_cnt[pass]) break;  // the whole bin is taken
   }
   } else {
@@ -556,6 +590,7 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
     }
   }
   __syncthreads();
+  if (kShared && tid == 0) SMQ_MARK(27);
   const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
@@ -637,10 +672,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
   if (tid == 32 * kQueryWarp) prefetch_tmap(&tm_q);
   if (kCopy && tid == 32 * 6) prefetch_tmap(&tm_k);
+  if (tid == 0) SMQ_MARK(0);
   // with programmatic dependent launch the prologue above overlaps the
   // previous kernel; everything below reads what earlier kernels wrote
   griddep_launch_dependents();
   griddep_wait();
+  if (tid == 0) SMQ_MARK(1);
   // tiles of row r: from its end, or (rows expanded here) the bound ceil(min(row_ke, S) / 256)
   const int per = (R + kScoreThreads - 1) / kScoreThreads;
   const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
@@ -685,6 +722,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int64_t t_begin = T * blockIdx.x / gridDim.x;
   const int64_t t_end = T * (blockIdx.x + 1) / gridDim.x;
   const int n = static_cast<int>(t_end - t_begin);
+  if (tid == 0) SMQ_MARK(2);
   if (n <= 0) return;
 
   // ---- TMEM: [acc 0 .. acc NA-1 | SF-A per stage (4 cols) | SF-B (4 cols)] ----
@@ -716,6 +754,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int spt = p.subs_per_tile;
   const int sbkv = p.sbkv;
   const int H = p.heads;
+  if (tid == 0) SMQ_MARK(3);
 
   if (warp == 0 && kFused) {
     // ======================= scheduler (rows expanded here) =======================
@@ -737,6 +776,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int ke = p.row_ke[r];
       int nkept = 0;
       const int cols = expand_row_in_warp(p, r, ke > 0 ? ke : 0, sorted, &nkept, lane);
+      if (lane == 0 && r == r_first) SMQ_MARK(4);
       // the CTA with the row's first tile writes its expansion, after the first
       // block-table loads are out so that the fence overlaps them
       bool pending_owner = row0 >= t_begin;
@@ -792,6 +832,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_desc_full(dslot));
+          if (lane == 0 && it == 0) SMQ_MARK(5);
+          if (lane == 0 && it == n - 1) SMQ_MARK(6);
           ++it;
         }
       }
@@ -875,6 +917,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_desc_full(dslot));
+        if (lane == 0 && it == 0) SMQ_MARK(5);
+        if (lane == 0 && it == n - 1) SMQ_MARK(6);
         ++it;
       }
     }
@@ -974,6 +1018,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                            g > 0);
           }
           mma_commit(bar_acc_full(a));
+          if (it == 0) SMQ_MARK(9);
+          if (it == n - 1) SMQ_MARK(10);
         }
         if (last_of_row) mma_commit(bar_q_empty(qb));
       }
@@ -1068,6 +1114,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int col = static_cast<int>(t - prefix[r]) * kTileM + h * kMmaM + m;
         if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
       }
+      if (warp == 2 && lane == 0 && ie == 0) SMQ_MARK(11);
+      if (warp == 2 && lane == 0 && ie == n - 1) SMQ_MARK(12);
       if (last_of_row) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty(qb));
@@ -1170,6 +1218,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
         __syncwarp();              // one arrival per warp
         if (lane == 0) mbar_arrive(bar_full(s));
+        if (warp == 6 && lane == 0 && j == 0) SMQ_MARK(7);
+        if (warp == 6 && lane == 0 && j == n - 1) SMQ_MARK(8);
       };
       auto load_tile = [&](uint4 (&vv)[kChunks], uint32_t (&ss)[kHalves], int i) {
         const SubBlockSrc* dring = desc + (i % kDescRing) * kMaxSubsPerTile;
@@ -1315,6 +1365,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // ---- teardown (TMEM is freed at the very end, so the top-k tail need not wait for it) ----
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) SMQ_MARK(13);
 
   // ---- top-k of the rows this CTA completed (their logits are in L2) ----
   if constexpr (kFused) {
@@ -1336,6 +1387,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if ((*end_src & kRowDone) == 0) continue;
         int32_t* e_clean = sm.sel + 12;  // the end without the flag
         if (tid == 0) *e_clean = *end_src & ~kRowDone;
+        if (tid == 0) SMQ_MARK(14);
         __syncthreads();
         const float* L = p.logits + static_cast<int64_t>(r) * S;
         int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
@@ -1347,6 +1399,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         else
           select_topk<kScoreThreads, 22, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
         __syncthreads();  // the scratch is reused by the next row
+        if (tid == 0) SMQ_MARK(15);
       }
     }
   }
@@ -1354,6 +1407,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+  if (tid == 0) SMQ_MARK(16);
 }
 
 // ===========================================================================
@@ -1428,6 +1482,564 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 }
 
 // ===========================================================================
+// Decode rows of a narrow batch: one thread-block cluster per row.
+// ===========================================================================
+// A cluster of C CTAs scores one row. Every CTA expands the row's candidate
+// blocks (the same result in each), and the row's tiles (the bound
+// ceil(min(row_ke, S) / 256), or ceil(end / 256) for an expansion passed in)
+// are split into C contiguous ranges, one per CTA. Each CTA runs the score
+// pipeline of the persistent kernel on its range, with the same warp roles,
+// and keeps its logits in shared memory. The other CTAs then store their
+// logits into CTA 0 (asynchronous stores through distributed shared memory,
+// one exchange), and CTA 0 selects the row's top-k there. No logits, counters
+// or atomics go through global memory.
+struct RowLayout {
+  uint32_t kv, q, sf, desc, w, bars, misc, sorted, sidx, lg, total;
+  __host__ __device__ RowLayout(int n_mma, int heads, int nsb, int num_cols) {
+    uint32_t o = 0;
+    kv = o;  // [stages][256 rows][128 B] keys; after the pipeline, top-k scratch
+    o += static_cast<uint32_t>(kScoreStages) * kTileM * kRowBytes;
+    q = o;  // [n_mma rows][128 B] E4M3 queries, 128-byte swizzle
+    o += static_cast<uint32_t>(n_mma) * kRowBytes;
+    sf = o;  // [stages][halves] key scale blocks of 512 B, then one block of 2^0
+    o += static_cast<uint32_t>(kScoreStages * kHalves + 1) * 512u;
+    desc = o;  // [ring][16 sub-blocks] source addresses
+    o += static_cast<uint32_t>(kDescRing) * kMaxSubsPerTile * sizeof(SubBlockSrc);
+    w = o;  // [heads] bf16 weights
+    o += round_up(static_cast<uint32_t>(heads) * 2u, 16);
+    bars = o;  // full, empty [stages]; acc_full, acc_empty [3]; q_full; drain [2]; setup; desc_full, desc_empty [ring];
+               // recv (the other CTAs' logits, in CTA 0)
+    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 4u + 2u * kDescRing + 1u) * 8u, 16);
+    misc = o;  // tmem base, abort flag, end, q_scale
+    o += 32u;
+    sorted = o;  // the row's kept candidate blocks, ascending
+    o += kMaxFusedBlocks * 4u;
+    sidx = o;  // [nsb] the row's sparse sub-block ids
+    o += round_up(static_cast<uint32_t>(nsb) * 4u, 16);
+    lg = o;  // [row columns] fp32 logits by sparse column: this CTA's, and in CTA 0 the whole row's
+    o += round_up(static_cast<uint32_t>(num_cols) * 4u, 16);
+    total = o;
+  }
+};
+
+size_t row_cluster_smem_bytes(int n_mma, int heads, int nsb, int num_cols) {
+  return RowLayout(n_mma, heads, nsb, num_cols).total + 1024;
+}
+
+template <int kN, int kJ>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    row_cluster_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ uint8_t rc_smem_raw[];
+  uint8_t* smem = align1024(rc_smem_raw);
+  constexpr int NS = kScoreStages;
+  constexpr int NA = acc_buffers(kN);
+  constexpr int kWarps = kScoreThreads / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = p.cluster;
+  const int r = blockIdx.x / C;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int S = p.num_cols;
+  const int sbkv = p.sbkv, spt = p.subs_per_tile;
+  const int H = p.heads;
+  const RowLayout lay(kN, H, p.nsb, S);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  auto bar_full = [&](int s) { return smem_addr(&bars[s]); };
+  auto bar_empty = [&](int s) { return smem_addr(&bars[NS + s]); };
+  auto bar_acc_full = [&](int a) { return smem_addr(&bars[2 * NS + a]); };
+  auto bar_acc_empty = [&](int a) { return smem_addr(&bars[2 * NS + kMaxAccBuffers + a]); };
+  constexpr int NB = 2 * NS + 2 * kMaxAccBuffers;
+  const uint32_t bar_q_full = smem_addr(&bars[NB]);
+  const uint32_t bar_drain = smem_addr(&bars[NB + 1]);  // and the next one
+  const uint32_t bar_setup = smem_addr(&bars[NB + 3]);
+  auto bar_desc_full = [&](int d) { return smem_addr(&bars[NB + 4 + d]); };
+  auto bar_desc_empty = [&](int d) { return smem_addr(&bars[NB + 4 + kDescRing + d]); };
+  auto bar_recv = [&](int pass) { return smem_addr(&bars[NB + 4 + 2 * kDescRing + pass]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
+  int32_t* end_sm = reinterpret_cast<int32_t*>(smem + lay.misc + 8);
+  float* qscale_sm = reinterpret_cast<float*>(smem + lay.misc + 12);
+  SubBlockSrc* desc = reinterpret_cast<SubBlockSrc*>(smem + lay.desc);
+  int32_t* sorted = reinterpret_cast<int32_t*>(smem + lay.sorted);
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem + lay.sidx);
+  float* lg = reinterpret_cast<float*>(smem + lay.lg);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full(s), kLoaderThreads / 32);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int d = 0; d < kDescRing; ++d) {
+      mbar_init(bar_desc_full(d), 1);
+      mbar_init(bar_desc_empty(d), kLoaderThreads / 32);
+    }
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(bar_acc_full(a), 1);
+      mbar_init(bar_acc_empty(a), kEpilogueThreads / 32);
+    }
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain + 8, 1);
+    mbar_init(bar_setup, 1);
+    mbar_init(bar_recv(0), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  // half of a cluster barrier: its other half, before the first store into
+  // another CTA, makes that CTA's barriers initialised
+  cluster_arrive();
+  if (tid == 0) SMQ_MARK(0);
+  // Until the previous kernel of the stream has finished, nothing it may have
+  // written is read: the row's inputs are only prefetched into L2 (address
+  // translations included), so that the loads after the wait hit there.
+  if (warp == 0) {
+    if (lane * 32 < p.ncb) prefetch_l2(p.candidate_blocks + static_cast<int64_t>(r) * p.ncb + lane * 32);
+    if (lane == 0) prefetch_l2(p.row_ke + r);
+    if (lane == 1 && p.row_indices) prefetch_l2(p.row_indices + r);
+    if (lane == 2) prefetch_l2(p.q_scale + r);
+    if (lane == 3 && !p.fused) prefetch_l2(p.end + r);
+    if (lane == 4) prefetch_l2(p.weights + static_cast<int64_t>(r) * H);
+    if (!p.fused)
+      for (int i = lane * 32; i < p.nsb; i += 32 * 32) prefetch_l2(p.sparse_indices + static_cast<int64_t>(r) * p.nsb + i);
+  } else if (warp == kQueryWarp && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tma_2d(&tm_q, 0, r * H);
+  } else if (warp == 2 && rank == 0) {
+    // the rows this cluster writes: their first lines (and address translations)
+    if (lane == 0) prefetch_l2(p.topk_out + static_cast<int64_t>(r) * p.topk_ld);
+    if (lane == 1 && p.col_indices) prefetch_l2(p.col_indices + static_cast<int64_t>(r) * p.topk);
+    if (lane == 2 && p.fused) prefetch_l2(p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb);
+    if (lane == 3 && p.fused) prefetch_l2(p.end_out + r);
+    if (lane == 4 && p.logits_out) prefetch_l2(p.logits_out + static_cast<int64_t>(r) * S);
+  } else if (warp >= 6 && warp < 10) {
+    // the block-table row of request r (the row's request when row_indices is the identity)
+    const int32_t* bt = p.block_table + static_cast<int64_t>(r < p.bt_rows ? r : 0) * p.bt_stride;
+    for (int i = (tid - 6 * 32) * 32; i < p.bt_stride; i += kLoaderThreads * 32) prefetch_l2(bt + i);
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  if (tid == 0) SMQ_MARK(1);
+
+  // this CTA's tiles of the row
+  int bound = p.fused ? p.row_ke[r] : p.end[r];
+  bound = bound < 0 ? 0 : (bound > S ? S : bound);
+  const int T = (bound + kTileM - 1) / kTileM;
+  const int t0 = static_cast<int>(static_cast<int64_t>(T) * rank / C);
+  const int n = static_cast<int>(static_cast<int64_t>(T) * (rank + 1) / C) - t0;
+  const int c0 = t0 * kTileM;  // the first sparse column of this CTA
+  if (tid == 0) SMQ_MARK(2);
+  // the scheduler's loads go out before the set-up below
+  int s_ke = 0, s_brow = 0, s_c0 = -1, s_c1 = -1;
+  if (warp == 0) {
+    s_ke = p.row_ke[r];
+    s_brow = p.row_indices ? p.row_indices[r] : r;
+    if (p.fused) {
+      const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * p.ncb;
+      s_c0 = lane < p.ncb ? cb[lane] : -1;
+      s_c1 = lane + 32 < p.ncb ? cb[lane + 32] : -1;
+    }
+  }
+
+  uint32_t tmem = 0;
+  if (n > 0) {
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
+    uint32_t* sf_one = reinterpret_cast<uint32_t*>(smem + lay.sf + kScoreStages * kHalves * 512);
+    if (tid < 128) sf_one[tid] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = *tmem_slot;
+    if (tid == 32) {
+      tmem_cp_32x128b_x4(tmem + NA * kHalves * kN + 4 * kHalves * NS, rows16_desc(smem_addr(sf_one)));
+      mma_commit(bar_setup);
+      if (!mbar_wait(bar_setup, 0, abort_flag, kWaitLimitNs)) {
+        set_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm_sfa = tmem + NA * kHalves * kN;
+  const uint32_t tm_sfb = tm_sfa + 4 * kHalves * NS;
+  if (tid == 0) SMQ_MARK(3);
+
+  if (warp == 0) {
+    // ======================= scheduler =======================
+    // The row's expansion into shared memory (expanded here, or the one passed
+    // in), then the source addresses of this CTA's sub-blocks, tile by tile.
+    const int64_t L = s_ke > 0 ? s_ke : 0;
+    const int brow = s_brow;
+    const int spb = p.cbs / sbkv;
+    int e = 0;
+    if (p.fused) {
+      int nkept = 0;
+      const int cols = expand_row_in_warp(p, L, s_c0, s_c1, sorted, &nkept, lane);
+      e = cols < 0 ? 0 : (cols > S ? S : cols);
+      for (int slot = lane; slot < p.nsb; slot += 32) {
+        const int k = slot / spb;
+        int v = -1;
+        if (k < nkept) {
+          const int sub = sorted[k] * spb + slot % spb;
+          if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
+        }
+        sidx[slot] = v;
+      }
+    } else {
+      e = p.end[r];
+      e = e < 0 ? 0 : (e > S ? S : e);
+      for (int slot = lane; slot < p.nsb; slot += 32) sidx[slot] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + slot];
+    }
+    if (lane == 0) st_volatile_s32(end_sm, e);
+    if (lane == 0) SMQ_MARK(4);
+    __syncwarp();  // sidx is read by every lane below
+    bool owner = p.fused && rank == 0;  // writes the row's expansion once its first block-table loads are out
+    bool ok = true;
+    int it = 0;
+    const int tiles_per_batch = 32 / spt;
+    for (int tb = 0; tb < n && ok; tb += tiles_per_batch) {
+      const int tl = tb + lane / spt;  // local tile
+      const int sub = lane % spt;
+      const int col_sub = (t0 + tl) * spt + sub;
+      const bool want = tl < n && col_sub * sbkv < e;
+      int pg = -1;
+      int64_t tpos = 0;
+      if (want) {
+        tpos = static_cast<int64_t>(sidx[col_sub]) * sbkv;
+        const int64_t slot = tpos / p.page_size;
+        if (sidx[col_sub] >= 0 && brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
+          pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
+      }
+      if (owner) {
+        for (int slot = lane; slot < p.nsb; slot += 32)
+          p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = sidx[slot];
+        if (lane == 0) p.end_out[r] = e;
+        owner = false;
+      }
+      int ntok = 0, trow = 0, tpage = 0;
+      const uint8_t* vsrc = nullptr;
+      const uint8_t* ssrc = nullptr;
+      if (want) {
+        if (pg >= 0 && pg < p.num_pages) {
+          const int64_t tok = tpos % p.page_size;
+          const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
+          vsrc = base + tok * (kHeadDim / 2);
+          ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
+          trow = static_cast<int>(tok);
+          tpage = pg;
+          ntok = sbkv;
+        } else {
+          set_status(p.status, kStatusBounds);
+        }
+      }
+      for (int k = 0; k < tiles_per_batch; ++k) {
+        if (tb + k >= n) break;
+        const int base = k * spt;
+        const int dslot = it % kDescRing;
+        bool e_ok = true;
+        if (lane == 0) e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane >= base && lane < base + spt)
+          put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_desc_full(dslot));
+        if (lane == 0 && it == 0) SMQ_MARK(5);
+        if (lane == 0 && it == n - 1) SMQ_MARK(6);
+        ++it;
+      }
+    }
+    if (owner) {  // a row with no tile in this CTA
+      for (int slot = lane; slot < p.nsb; slot += 32)
+        p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = sidx[slot];
+      if (lane == 0) p.end_out[r] = e;
+    }
+    if (!ok) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (warp == kQueryWarp) {
+    // ======================= query loader =======================
+    if (lane == 0 && n > 0) {
+      *qscale_sm = p.q_scale[r];
+      mbar_arrive_expect_tx(bar_q_full, kN * kRowBytes + H * 2);
+      tma_load_2d(smem_addr(smem + lay.q), &tm_q, 0, r * H, bar_q_full);
+      bulk_load(smem_addr(smem + lay.w), p.weights + static_cast<int64_t>(r) * H, H * 2, bar_q_full);
+      const volatile int never = 0;
+      mbar_wait(bar_q_full, 0, &never, kWaitLimitNs);  // the copies land before the CTA can exit
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ======================= MMA issuers (alternate tiles) =======================
+    const int par = warp == 1 ? 0 : 1;
+    if (lane == 0 && n > 0) {
+      uint32_t idesc[4];
+      for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kMmaM, kN, g, g);
+      bool ok = mbar_wait(bar_q_full, 0, abort_flag, kWaitLimitNs);
+      const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q));
+      for (int it = 0; it < n && ok; ++it) {
+        if (NA > 1 ? ((it & 1) != par) : (par != 0)) continue;
+        const int s = it % NS;
+        const int a = it % NA;
+        ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t stage_addr = smem_addr(smem + lay.kv + s * (kTileM * kRowBytes));
+        for (int h = 0; h < kHalves; ++h) {
+          const uint32_t sfa = tm_sfa + 4 * (s * kHalves + h);
+          tmem_cp_32x128b_x4(sfa, rows16_desc(smem_addr(smem + lay.sf + (s * kHalves + h) * 512)));
+          const uint64_t adesc = sw128_desc(stage_addr + h * (kMmaM * kRowBytes));
+          for (int g = 0; g < 4; ++g)
+            mma_mxf8f6f4(tmem + (a * kHalves + h) * kN, adesc + 2 * g, bdesc + 2 * g, idesc[g], sfa, tm_sfb, g > 0);
+        }
+        mma_commit(bar_acc_full(a));
+        if (it == 0) SMQ_MARK(9);
+        if (it == n - 1) SMQ_MARK(10);
+      }
+      if (!ok) {
+        set_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      const uint32_t drain = bar_drain + 8 * par;
+      mma_commit(drain);
+      const volatile int never = 0;
+      mbar_wait(drain, 0, &never, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ======================= epilogue (warps 2..5) =======================
+    // One TMEM lane (one key position of each half) per thread. The logit goes
+    // to shared memory (and the caller's logits_out), and its top 12 bits are
+    // counted for the top-k.
+    const int q4 = warp & 3;
+    const int m = 32 * q4 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    bool ok = n > 0 ? warp_wait(bar_q_full, 0, abort_flag, kWaitLimitNs) : true;
+    float w[kN];
+    const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w);
+#pragma unroll
+    for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+    const float qs = n > 0 ? *qscale_sm : 0.f;
+    float* lout = p.logits_out ? p.logits_out + static_cast<int64_t>(r) * S : nullptr;
+    int e = 0;
+    for (int ie = 0; ie < n && ok; ++ie) {
+      const int a = ie % NA;
+      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
+      if (!ok) break;
+      if (ie == 0) e = ld_volatile_s32(end_sm);  // written before the first tile was published
+      if (warp == 2 && lane == 0) mbar_arrive(bar_empty(ie % NS));
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t tacc = tmem + (a * kHalves + h) * kN + lane_base;
+#pragma unroll
+        for (int c = 0; c < kN; c += 32) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tacc + c, v0);
+          tmem_ld16(tacc + c + 16, v1);
+          tmem_wait_ld();
+          if (h == kHalves - 1 && c + 32 >= kN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty(a));
+          }
+#pragma unroll
+          for (int hh = 0; hh < 16; ++hh)
+            acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+#pragma unroll
+          for (int hh = 0; hh < 16; ++hh)
+            acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
+        }
+        const float logit = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * qs;
+        const int lc = ie * kTileM + h * kMmaM + m;  // local column
+        const int col = c0 + lc;
+        if (col < e) lg[col] = logit;
+        if (lout && col < S) lout[col] = col < e ? logit : -INFINITY;
+      }
+      if (warp == 2 && lane == 0 && ie == 0) SMQ_MARK(11);
+      if (warp == 2 && lane == 0 && ie == n - 1) SMQ_MARK(12);
+    }
+    if (!ok) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  } else if (warp >= 6 && warp < 10) {
+    // ======================= loaders (warps 6..9) =======================
+    // Coalesced 16-byte loads two tiles ahead into registers, then stores into
+    // the MMA's padded containers (as in the persistent kernel).
+    constexpr int kChunks = kTileM / 32;
+    const int q4 = warp & 3;
+    const int m = 32 * q4 + lane;
+    const uint32_t sf_base = smem_addr(smem + lay.sf);
+    const uint32_t kv_base = smem_addr(smem + lay.kv);
+    const int vch = m & 3;
+    int vu[kChunks], vtk[kChunks];
+#pragma unroll
+    for (int k8 = 0; k8 < kChunks; ++k8) {
+      const int pos = (m >> 2) + 32 * k8;
+      vu[k8] = pos / sbkv;
+      vtk[k8] = pos % sbkv;
+    }
+    int su[kHalves], stk[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      su[h] = (m + h * kMmaM) / sbkv;
+      stk[h] = (m + h * kMmaM) % sbkv;
+    }
+    uint4 v[2][kChunks];
+    uint32_t sw[2][kHalves];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) v[k][k8] = make_uint4(0u, 0u, 0u, 0u);
+    auto store_tile = [&](const uint4 (&vv)[kChunks], const uint32_t (&ss)[kHalves], int j) {
+      const int s = j % NS;
+      const uint32_t stage = kv_base + s * (kTileM * kRowBytes);
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) {
+        const int pos = (m >> 2) + 32 * k8;
+        const uint32_t dst = stage + static_cast<uint32_t>(pos) * kRowBytes;
+        const uint32_t swz = static_cast<uint32_t>(pos & 7);
+        sts_v2(dst + (((2 * vch) ^ swz) << 4), vv[k8].x, vv[k8].y);
+        sts_v2(dst + (((2 * vch + 1) ^ swz) << 4), vv[k8].z, vv[k8].w);
+      }
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full(s));
+      if (warp == 6 && lane == 0 && j == 0) SMQ_MARK(7);
+      if (warp == 6 && lane == 0 && j == n - 1) SMQ_MARK(8);
+    };
+    auto load_tile = [&](uint4 (&vv)[kChunks], uint32_t (&ss)[kHalves], int i) {
+      const SubBlockSrc* dring = desc + (i % kDescRing) * kMaxSubsPerTile;
+#pragma unroll
+      for (int k8 = 0; k8 < kChunks; ++k8) {
+        const SubBlockSrc d = get_src(dring + vu[k8]);
+        ldg_stream_v4_if(vv[k8], d.values + static_cast<int64_t>(vtk[k8]) * (kHeadDim / 2) + 16 * vch,
+                         d.values != nullptr && vtk[k8] < d.positions);
+      }
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        const SubBlockSrc ds = get_src(dring + su[h]);
+        ss[h] = 0x7F7F7F7Fu;
+        ldg_stream_u32_if(ss[h], ds.scales + static_cast<int64_t>(stk[h]) * kScaleWordBytes,
+                          ds.values != nullptr && stk[h] < ds.positions);
+      }
+    };
+    bool ok = true;
+    for (int i0 = 0; i0 < n + 2 && ok; i0 += 2) {
+      const int j0 = i0 - 2;
+      if (j0 >= 0 && j0 < n) {
+        const int jl = j0 + 1 < n ? j0 + 1 : j0;
+        ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        store_tile(v[0], sw[0], j0);
+        if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
+      }
+      if (i0 < n) {
+        const int il = i0 + 1 < n ? i0 + 1 : i0;
+        bool both = false;
+        if (lane == 0) both = mbar_test_wait(bar_desc_full(il % kDescRing), (il / kDescRing) & 1);
+        both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
+        __syncwarp();
+        if (!both) {
+          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+        }
+        load_tile(v[0], sw[0], i0);
+        if (i0 + 1 < n) {
+          if (!both) {
+            ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+          }
+          load_tile(v[1], sw[1], i0 + 1);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_desc_empty(i0 % kDescRing));
+          if (i0 + 1 < n) mbar_arrive(bar_desc_empty((i0 + 1) % kDescRing));
+        }
+      }
+    }
+    if (!ok) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) SMQ_MARK(13);
+  if (n > 0 && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+
+  // ---- top-k: the other CTAs' logits into CTA 0, which selects ----
+  // Each other CTA stores its valid logits into CTA 0's row of logits
+  // (asynchronous stores completing on CTA 0's barrier) and leaves. CTA 0
+  // then selects on shared memory alone. Every CTA computes the same `end`, so
+  // all take the same branch.
+  const int e = ld_volatile_s32(end_sm);
+  const int k = p.topk;
+  int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
+  int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr;
+  if (rank == C - 1 && p.logits_out)  // columns past the last tile
+    for (int c = T * kTileM + tid; c < S; c += kScoreThreads) p.logits_out[static_cast<int64_t>(r) * S + c] = -INFINITY;
+  auto valid_cols = [&](int cr) {  // valid columns of CTA cr: [T cr / C * 256, ...) below e
+    const int a = static_cast<int>(static_cast<int64_t>(T) * cr / C) * kTileM;
+    const int b = static_cast<int>(static_cast<int64_t>(T) * (cr + 1) / C) * kTileM;
+    const int hi = b < e ? b : e;
+    return hi > a ? hi - a : 0;
+  };
+  const bool select = e > k;
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  if (rank != 0) {
+    if (select) {
+      const int nv = valid_cols(rank);
+      const uint32_t src = smem_addr(lg + c0), bar = bar_recv(0);
+      for (int i = tid; 4 * i + 3 < nv; i += kScoreThreads)
+        st_async_v4(src + 16u * i, 0, *reinterpret_cast<const uint4*>(lg + c0 + 4 * i), bar);
+      for (int c = (nv & ~3) + tid; c < nv; c += kScoreThreads)
+        st_async_u32(src + 4u * c, 0, __float_as_uint(lg[c0 + c]), bar);
+    }
+    return;
+  }
+  if (!select) {  // every valid column is selected, in column order
+    const int sb_shift = 31 - __clz(sbkv);
+    for (int c = tid; c < k; c += kScoreThreads) {
+      out[c] = c < e ? (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1)) : -1;
+      if (colo) colo[c] = c < e ? c : -1;
+    }
+    if (tid == 0) SMQ_MARK(16);
+    return;
+  }
+  int incoming = 0;
+  for (int cr = 1; cr < C; ++cr) incoming += valid_cols(cr);
+  if (tid == 0) mbar_arrive_expect_tx(bar_recv(0), static_cast<uint32_t>(incoming) * 4u);
+  fence_proxy_async_smem();  // the key stages (written for the tensor core) become plain scratch
+  uint8_t* scr = smem + lay.kv;
+  TopkScratch sm;
+  sm.hist = reinterpret_cast<uint32_t*>(scr);
+  sm.bsum = nullptr;
+  sm.wsum = reinterpret_cast<int*>(scr + kTopkBins * 4);
+  sm.chunk = reinterpret_cast<uint32_t*>(sm.wsum + 32);
+  sm.sel = reinterpret_cast<int*>(sm.chunk + 32 * 32);
+  sm.sidx = sidx;
+  if (!warp_wait(bar_recv(0), 0, abort_flag, kWaitLimitNs)) set_status(p.status, kStatusTimeout);
+  if (tid == 0) SMQ_MARK(14);
+  select_topk<kScoreThreads, kJ, true, true>(lg, S, end_sm, k, nullptr, p.nsb, sbkv, out, colo, nullptr, sm);
+  if (tid == 0) SMQ_MARK(16);
+}
+
+// ===========================================================================
 // Launchers
 // ===========================================================================
 cudaError_t prepare_kernels(int n_mma) {
@@ -1462,6 +2074,17 @@ cudaError_t prepare_kernels(int n_mma) {
   for (int i = 0; i < 7; ++i) {
     if ((i < 4) != (n_mma == 64)) continue;
     err = cudaFuncSetAttribute(score[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (err != cudaSuccess) return err;
+  }
+  const void* rc[] = {reinterpret_cast<const void*>(&row_cluster_kernel<64, 11>),
+                      reinterpret_cast<const void*>(&row_cluster_kernel<64, 22>),
+                      reinterpret_cast<const void*>(&row_cluster_kernel<128, 11>),
+                      reinterpret_cast<const void*>(&row_cluster_kernel<128, 22>)};
+  for (int i = 0; i < 4; ++i) {
+    if ((i < 2) != (n_mma == 64)) continue;
+    err = cudaFuncSetAttribute(rc[i], cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(rc[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
   }
   if (err != cudaSuccess) return err;
@@ -1524,6 +2147,32 @@ cudaError_t launch_score(const ScoreParams& p, bool paged, bool copy, const CUte
   if (stat) return launch_pdl_n(score_kernel<true, 128, true>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
   if (paged) return launch_pdl_n(score_kernel<true, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
   return launch_pdl_n(score_kernel<false, 128, false>, grid, kScoreThreads, smem, stream, p, tm_q, tm_k);
+}
+
+template <int kN, int kJ>
+cudaError_t launch_rc(const ScoreParams& p, const CUtensorMap& tm_q, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.rows) * static_cast<unsigned>(p.cluster));
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, row_cluster_kernel<kN, kJ>, p, tm_q);
+}
+
+cudaError_t launch_row_cluster(const ScoreParams& p, const CUtensorMap& tm_q, size_t smem, cudaStream_t stream) {
+  const bool narrow = p.num_cols <= kScoreThreads * 11;  // keys per thread of the selection
+  static_assert(kScoreThreads * 22 >= kRowClusterMaxCols, "the widest row's keys fit the selection");
+  if (p.n_mma == 64) return narrow ? launch_rc<64, 11>(p, tm_q, smem, stream) : launch_rc<64, 22>(p, tm_q, smem, stream);
+  return narrow ? launch_rc<128, 11>(p, tm_q, smem, stream) : launch_rc<128, 22>(p, tm_q, smem, stream);
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {

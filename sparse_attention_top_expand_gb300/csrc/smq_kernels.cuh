@@ -50,6 +50,20 @@ constexpr int kMaxSparseCols = 16384;
 constexpr int kStatusBounds = 8;    // SMQ_ERR_BOUNDS
 constexpr int kStatusTimeout = 16;  // SMQ_ERR_TIMEOUT
 
+// Tracing build (-DSMQ_TRACE, a separate library; see include/smq_trace.h):
+// the score kernel stamps %globaltimer at its phase boundaries into a device
+// array of kTraceSlots stamps per CTA. In the product build every mark
+// compiles to nothing.
+#ifdef SMQ_TRACE
+constexpr int kTraceSlots = 32;
+constexpr int kTraceCtas = 1024;
+cudaError_t trace_read(uint64_t* host, size_t count);
+cudaError_t trace_clear();
+#define SMQ_MARK(slot) ::smq::trace_mark(slot)
+#else
+#define SMQ_MARK(slot) ((void)0)
+#endif
+
 // Everything the fused gather + score kernel reads besides its tensor maps.
 struct ScoreParams {
   int32_t rows;
@@ -97,6 +111,9 @@ struct ScoreParams {
   int32_t* topk_out;     // [rows][topk_ld]
   int32_t* col_indices;  // [rows][topk], may be null
   float* logits_fill;    // when non-null: -inf into columns >= end (the caller's logits_out)
+  // row-cluster kernel: CTAs per row (the cluster size); logits_out, or null
+  int32_t cluster;
+  float* logits_out;
   // outputs
   float* logits;     // [rows][num_cols]
   int32_t* status;   // workspace status word
@@ -148,9 +165,18 @@ struct GatherParams {
 // Shared-memory bytes of the score kernel for a geometry.
 size_t score_smem_bytes(int n_mma, int heads, int rows);
 
+// The row-cluster decode kernel: one cluster of at most kRowClusterMaxCtas
+// CTAs per row, for rows of at most kRowClusterMaxCols sparse columns. Its
+// shared-memory bytes:
+constexpr int kRowClusterMaxCols = 8192;
+constexpr int kRowClusterMaxCtas = 8;
+size_t row_cluster_smem_bytes(int n_mma, int heads, int nsb, int num_cols);
+
 cudaError_t launch_expand(const ExpandParams& p, cudaStream_t stream);
 cudaError_t launch_score(const ScoreParams& p, bool paged, bool copy, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                          int grid, size_t smem, cudaStream_t stream);  // paged with p.fused: rows expanded in the kernel
+cudaError_t launch_row_cluster(const ScoreParams& p, const CUtensorMap& tm_q, size_t smem,
+                               cudaStream_t stream);  // grid = rows x p.cluster
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
