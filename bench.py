@@ -214,6 +214,8 @@ def load_traffic(workload: str, kernel: str):
 
 def make_inputs(workload: str, rank: int):
     from sparse_attention_top_expand_gb300 import synth
+    if workload == "tiny_decode":
+        return synth.tiny_decode(seed=rank_seed(0, rank))
     if workload == "decode_batch":
         return synth.decode_batch(seed=rank_seed(1, rank))
     if workload == "long_context_decode":
@@ -254,28 +256,50 @@ def valid_cols(inp, plan) -> int:
 # ------------------------------------------------------------------ our arm
 
 
-def run_ours(args, rank, world, dist):
+def launches_per_step(workload: str, plan, rows: int, layers: int) -> int:
+    """Kernel launches of the library in one step of a workload."""
+    ncb = plan.candidate_topk_blocks
+    if workload == "prefill_chunk":
+        return 4  # gather, expansion, score, top-k
+    # paged decode: one cluster per row (one launch, +1 expansion kernel past 64 blocks) for
+    # no more rows than SMs, else the persistent score kernel (expansion inside up to 64
+    # blocks) and the top-k kernel
+    if rows <= plan.num_sms and plan.num_sparse_cols <= 8192:
+        per_call = 1 if ncb <= 64 else 2
+    else:
+        per_call = 2 if ncb <= 64 else 3
+    if workload == "shared_schedule":
+        return 1 + layers  # one shared expansion, then one cluster kernel per consumer layer
+    return per_call
+
+
+def algorithmic_bytes(inp, plan, cols: int, nsub: int) -> int:
+    """Bytes a decode step must move: 68 B per valid column (FP4 values and UE8M0 scales), per row
+    its Q, scale, weights, top-k ids and candidate ids, and one block-table word per sub-block."""
+    g = inp.geom
+    per_row = g.num_heads * g.head_dim + 4 + 2 * g.num_heads + 4 * g.topk + 4 * g.candidate_topk_blocks
+    return cols * 68 + inp.rows * per_row + 4 * nsub
+
+
+def measure(workload, args, rank, world, dist, device, steps, warmup, headline):
+    """Time `steps` graph-replayed steps of one workload; returns its result fields."""
     import torch
 
     import sparse_attention_top_expand_gb300 as smq
     from sparse_attention_top_expand_gb300 import tensors
 
-    _, _, local = dist_info()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    inp = make_inputs(args.workload, rank)
+    local = device.index
+    inp = make_inputs(workload, rank)
     layers = inp if isinstance(inp, list) else [inp]
     base = layers[0]
     plan = tensors.plan_for(base.geom, max_rows=base.rows, device=local)
     cols = valid_cols(base, plan)
     rows = base.rows
-    prefill = args.workload == "prefill_chunk"
+    prefill = workload == "prefill_chunk"
+    shared = workload == "shared_schedule"
 
     # replicas: enough independent copies that one cycle touches > 4x L2
-    if prefill:
-        touched = cols * 68 + rows * base.geom.num_heads * 128
-    else:
-        touched = cols * 68 + rows * base.geom.num_heads * 128
+    touched = cols * 68 + rows * base.geom.num_heads * 128
     nrep = args.replicas or max(2, min(64, math.ceil(4 * L2_BYTES / max(touched * len(layers), 1))))
     Dev = tensors.PrefillDevice if prefill else tensors.DecodeDevice
     reps = [[Dev(x, plan, with_logits=False, with_cols=False) for x in layers] for _ in range(nrep)]
@@ -283,20 +307,30 @@ def run_ours(args, rank, world, dist):
         for rep in reps:
             rep[0].gather(plan)
     torch.cuda.synchronize()
-
-    if args.workload == "shared_schedule":
-        # every consumer layer reads the first layer's expansion buffers
+    if shared:  # every consumer layer reads the first layer's expansion buffers
         for rep in reps:
             for d in rep[1:]:
                 d.sparse_indices = rep[0].sparse_indices
                 d.end = rep[0].end
 
+    rt = cuda_runtime()
+
+    def mark(ev):  # an event record that a stream capture keeps as a graph node
+        if ev is not None:
+            rc = rt.cudaEventRecordWithFlags(ev.cuda_event, torch.cuda.current_stream().cuda_stream, 1)
+            if rc:
+                raise SystemExit(f"cudaEventRecordWithFlags failed ({rc})")
+
     def step(i, events=None):
         rep = reps[i % nrep]
-        if args.workload == "shared_schedule":
+        if shared:
+            ev = events or [None] * (2 + len(rep))
+            mark(ev[0])
             rep[0].expand(plan)
-            for d in rep:
+            mark(ev[1])
+            for li, d in enumerate(rep):
                 d.run(plan, expansion_ready=True)
+                mark(ev[2 + li])
             return
         d = rep[0]
         if prefill:
@@ -309,56 +343,50 @@ def run_ours(args, rank, world, dist):
                                               d.row_indices, d.row_ke, d.candidate_blocks, d.topk_out,
                                               d.sparse_indices, d.end, d.workspace, profile_events=events)
 
-    # decode rows with at most 64 candidate blocks are expanded inside the score kernel, which also
-    # selects their top-k when a row has at most 8448 sparse columns
-    if base.geom.candidate_topk_blocks <= 64:
-        decode_launches = 1 if plan.num_sparse_cols <= 8448 and 2 * rows <= plan.num_sms else 2
-    else:
-        decode_launches = 3
-    launches_per_step = {"decode_batch": decode_launches, "long_context_decode": decode_launches,
-                         "prefill_chunk": 4, "prefill_chunk_paged": decode_launches,
-                         "shared_schedule": 1 + 2 * len(layers)}[args.workload]
-
-    for i in range(args.warmup):
+    launches = launches_per_step(workload, plan, rows, len(layers))
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     for rep in reps:
         for d in rep:
             st = smq.smq_get_status(d.workspace)
             if st:
-                raise SystemExit(f"device status {st} during warm-up")
+                raise SystemExit(f"{workload}: device status {st} during warm-up")
 
-    # graph of G steps, one pass over the replicas. Every EVENT_EVERY-th step records its kernel
-    # boundaries with events inside the graph: an event node costs about 2 us of serialisation,
-    # so instrumenting every step would slow the timed region it measures. Stages that run
-    # inside the score kernel get no events of their own.
-    G = min(nrep, args.steps) if args.steps > 0 else 1
-    fused_expand = not prefill and base.geom.candidate_topk_blocks <= 64
-    fused_topk = fused_expand and decode_launches == 1
-    timed = [j for j in range(G) if j % EVENT_EVERY == 0]
-    evs = {j: [None if fused_expand else timing_event(torch), timing_event(torch), timing_event(torch),
-               None if fused_topk else timing_event(torch)] for j in timed}
+    # graph of G steps, one pass over the replicas. Every EVENT_EVERY-th step records
+    # its kernel boundaries with events inside the graph: an event node costs about
+    # 2 us of serialisation, so only some steps carry them.
+    G = min(nrep, steps) if steps > 0 else 1
+    nev = 2 + len(layers) if shared else 4
+    timed = [j for j in range(G) if j % EVENT_EVERY == 0] if (rt is not None or not shared) else []
+    evs = {j: [timing_event(torch) for _ in range(nev)] for j in timed}
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for j in range(G):
-            step(j, evs.get(j) if args.workload != "shared_schedule" else None)
-    rem = args.steps % G
+            step(j, evs.get(j))
+    rem = steps % G
     graph_rem = None
     if rem:
         graph_rem = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_rem):
             for j in range(rem):
                 step(j)
-    reps_full = args.steps // G
+    reps_full = steps // G
 
-    clocks = ClockSampler(gpu_smi_id(local))
+    # clocks: sampled from a load burst of the same graph just before the timed
+    # region through its end, so that even a short timed region has a record
+    clocks = ClockSampler(gpu_smi_id(local)) if headline else None
     barrier(dist, device)
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.6)
+    if clocks:
+        clocks.start()
+        first = clocks.mark()
+        t_end = time.perf_counter() + 0.4
+        while time.perf_counter() < t_end:
+            graph.replay()
+            torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    first = clocks.mark()
     t0.record()
     for _ in range(reps_full):
         graph.replay()
@@ -366,81 +394,137 @@ def run_ours(args, rank, world, dist):
         graph_rem.replay()
     t1.record()
     torch.cuda.synchronize()
-    last = clocks.mark()
-    clk = clocks.stop(first, last)
+    clk = None
+    if clocks:
+        time.sleep(0.12)
+        clk = clocks.stop(first, clocks.mark())
     barrier(dist, device)
     ms = t0.elapsed_time(t1)
-    value, ms_max, total_cols = aggregate(cols * args.steps, ms, dist, device)
-    total_rows = reduce_sum(rows * args.steps, dist, device)
+    value, ms_max, _ = aggregate(cols * steps, ms, dist, device)
+    total_rows = reduce_sum(rows * steps, dist, device)
+    ms_step = ms_max / steps
 
-    # per-kernel durations: the events of the last graph replay (G launches)
     kernel_ms = None
-    if args.workload != "shared_schedule" and reps_full:
+    if reps_full and evs:
+        ev = list(evs.values())
         try:
-            ev = list(evs.values())
-            kernel_ms = {
-                "expand": 0.0 if fused_expand else statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
-                "score": statistics.mean(e[1].elapsed_time(e[2]) for e in ev),
-                "topk": 0.0 if fused_topk else statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
-                "source": f"CUDA events inside the timed graph, last replay ({len(ev)} of its {G} launches)"
-                          + ("; expansion" + (" and top-k" if fused_topk else "") + " run inside the score kernel"
-                             if fused_expand else ""),
-            }
+            if shared:
+                kernel_ms = {
+                    "expand": statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+                    "per_layer": statistics.mean(e[1].elapsed_time(e[-1]) / len(layers) for e in ev),
+                    "layers": [statistics.mean(e[1 + li].elapsed_time(e[2 + li]) for e in ev)
+                               for li in range(len(layers))],
+                }
+            else:
+                # a stage that runs inside the score kernel has no launch of its own: its two events
+                # are back to back and would time only their own overhead
+                separate_expand = prefill or (launches == 3) or (launches == 2 and rows <= plan.num_sms)
+                separate_topk = launches > 1 and not (launches == 2 and rows <= plan.num_sms)
+                kernel_ms = {"expand": statistics.mean(e[0].elapsed_time(e[1]) for e in ev) if separate_expand else 0.0,
+                             "score": statistics.mean(e[1].elapsed_time(e[2]) for e in ev),
+                             "topk": statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if separate_topk else 0.0}
+            kernel_ms["source"] = (f"CUDA events inside the timed graph, last replay ({len(ev)} of its {G} steps); "
+                                   "0 for a stage that runs inside the score kernel")
         except (RuntimeError, ValueError):
-            kernel_ms = eager_kernel_times(step, G, torch)
+            kernel_ms = None
     for rep in reps:
         for d in rep:
             st = smq.smq_get_status(d.workspace)
             if st:
-                raise SystemExit(f"device status {st} after the timed region")
-
-    # end to end through the public API with host buffers
-    e2e = run_e2e(args, plan, base, cols, dist, device) if args.workload in ("decode_batch",
-                                                                              "long_context_decode") else None
+                raise SystemExit(f"{workload}: device status {st} after the timed region")
 
     peaks, peak_src = load_peaks()
     roof = None
-    if kernel_ms:
-        g = base.geom
-        nsub = sum(int(x) for x in (reps[0][0].end.cpu().numpy() + plan.sparse_block_kv - 1) // plan.sparse_block_kv)
-        if prefill or args.workload == "prefill_chunk_paged":  # a contraction-bound chunk
+    g = base.geom
+    if kernel_ms and not shared:
+        if prefill or workload == "prefill_chunk_paged":  # a contraction-bound chunk
             flops = 2.0 * g.num_heads * g.head_dim * cols
-            achieved = flops / (kernel_ms["score"] / 1e3) / 1e12
-            peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+            t = min(kernel_ms["score"], ms_step) / 1e3
+            achieved = flops / t / 1e12
+            bf16 = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+            peak = 2.0 * bf16
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": load_traffic(args.workload, "score_kernel"),
-                    "peak_source": f"{peak_src}: 2 x sustained bf16 (fp8 x fp4 runs at the fp8 dense rate)",
-                    "algorithmic_flops_per_launch": flops}
+                    "frac": achieved / peak, "traffic": load_traffic(workload, "score_kernel"),
+                    "peak_source": f"{peak_src}: 2 x sustained bf16 (fp8 x fp4 block-scaled runs at the fp8 rate)",
+                    "frac_of_fp4_rate": achieved / (6.0 * bf16),
+                    "algorithmic_flops_per_launch": flops, "kernel": "score_kernel"}
         else:
-            alg = cols * 68 + rows * (g.num_heads * g.head_dim + 2 * g.num_heads + 4) + 4 * nsub
-            achieved = alg / (kernel_ms["score"] / 1e3) / 1e9
+            nsub = sum(int(x) for x in (reps[0][0].end.cpu().numpy() + plan.sparse_block_kv - 1)
+                       // plan.sparse_block_kv)
+            alg = algorithmic_bytes(base, plan, cols, nsub)
+            one_launch = launches == 1
+            t = (ms_step if one_launch else min(kernel_ms["score"], ms_step)) / 1e3
+            achieved = alg / t / 1e9
             peak = peaks["hbm_gbs"]
-            roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": load_traffic(args.workload, "score_kernel"),
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": load_traffic(workload, "row_cluster_kernel" if one_launch else "score_kernel"),
                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": alg,
-                    "kernel": "score_kernel (fused expansion, gather, tcgen05 mxf8f6f4, epilogue"
-                              + (", top-k)" if decode_launches == 1 else ")")}
+                    "time": "step time (one launch per step)" if one_launch
+                            else "score kernel events, at most the step time",
+                    "kernel": "row_cluster_kernel (expansion, gather, tcgen05 mxf8f6f4, epilogue, top-k)"
+                              if one_launch else "score_kernel (expansion, gather, tcgen05 mxf8f6f4, epilogue)"}
+    elif kernel_ms and shared:
+        nsub = sum(int(x) for x in (reps[0][0].end.cpu().numpy() + plan.sparse_block_kv - 1)
+                   // plan.sparse_block_kv)
+        alg = algorithmic_bytes(base, plan, cols, nsub)
+        t = min(kernel_ms["per_layer"], ms_step) / 1e3
+        roof = {"bound": "hbm", "achieved": alg / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": alg / t / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": alg,
+                "time": "mean consumer-layer launch (events inside the timed graph)",
+                "kernel": "row_cluster_kernel per consumer layer"}
 
-    cpu = run_cpu_baseline(args, base, rank) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    decode_like = workload in ("decode_batch", "long_context_decode", "tiny_decode")
+    e2e = run_e2e(args, plan, base, cols, dist, device) if (decode_like and args.e2e_steps > 0) else None
+    cpu = (run_cpu_baseline(base, workload, args.cpu_seconds if headline else args.cpu_seconds / 2)
+           if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None)
 
     extra = {"rows": rows, "cols_per_step": cols, "replicas": nrep, "graph_steps": G,
              "l2": f"{nrep} rotating input replicas, ~{touched * len(layers) * nrep / 1e6:.0f} MB touched per cycle "
                    f"(> 4x L2); no flush"}
-    if args.workload == "shared_schedule":
+    if shared:
         extra["layers"] = len(layers)
+    out = {
+        "value": value, "unit": UNIT, "ms_per_step": ms_step, "rows_per_s": total_rows / (ms_max / 1e3),
+        "config": workload_config(workload, layers, plan, extra),
+        "kernel_ms": kernel_ms, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * steps, "steps": steps,
+    }
+    if clk is not None:
+        out["clocks"] = clk
+    return out
+
+
+WORKLOAD_STEPS = {"tiny_decode": 400, "decode_batch": 400, "long_context_decode": 200, "prefill_chunk": 40,
+                  "prefill_chunk_paged": 40, "shared_schedule": 200}
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    _, _, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    head = measure(args.workload, args, rank, world, dist, device, args.steps, args.warmup, headline=True)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8 e4m3 x fp4 e2m1 (ue8m0 block scales), fp32 accumulate, fp32 logits",
         "data": "synthetic (seeded generator; no dataset)",
-        "config": workload_config(args.workload, layers, plan, extra),
-        "rows_per_s": total_rows / (ms_max / 1e3),
-        "kernel_ms": kernel_ms, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-        "gpu_launches": launches_per_step * args.steps,
+        "config": head["config"], "rows_per_s": head["rows_per_s"], "kernel_ms": head["kernel_ms"],
+        "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+        "clocks": head.get("clocks"), "gpu_launches": head["gpu_launches"],
     }
-    if args.workload == "shared_schedule":
-        line.update(shared_schedule_split(args, plan, reps))
+    if not args.no_workloads:
+        others = {}
+        for w in ("tiny_decode", "long_context_decode", "prefill_chunk", "prefill_chunk_paged", "shared_schedule",
+                  "decode_batch"):
+            if w == args.workload:
+                continue
+            others[w] = measure(w, args, rank, world, dist, device, WORKLOAD_STEPS[w], max(3, args.warmup),
+                                headline=False)
+        line["workloads"] = others
     return line
 
 
@@ -457,8 +541,9 @@ def cuda_runtime():
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         rt.cudaStreamWaitEvent.argtypes = [vp, vp, ctypes.c_uint]
         rt.cudaEventRecord.argtypes = [vp, vp]
+        rt.cudaEventRecordWithFlags.argtypes = [vp, vp, ctypes.c_uint]
         rt.cudaMemcpyAsync.argtypes = [vp, vp, sz, ctypes.c_int, vp]
-        for f in (rt.cudaStreamWaitEvent, rt.cudaEventRecord, rt.cudaMemcpyAsync):
+        for f in (rt.cudaStreamWaitEvent, rt.cudaEventRecord, rt.cudaEventRecordWithFlags, rt.cudaMemcpyAsync):
             f.restype = ctypes.c_int
         return rt
     return None
@@ -472,18 +557,6 @@ def timing_event(torch):
     return ev
 
 
-def eager_kernel_times(step, n, torch):
-    """Kernel durations from CUDA events on eager (uncaptured) calls."""
-    evs = [[timing_event(torch) for _ in range(4)] for _ in range(n)]
-    for j in range(n):
-        step(j, evs[j])
-    torch.cuda.synchronize()
-    return {"expand": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-            "score": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-            "topk": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
-            "source": f"CUDA events on {n} eager calls after the timed region"}
-
-
 def gpu_smi_id(local: int) -> str:
     """The nvidia-smi id of CUDA device `local` (by UUID)."""
     import torch
@@ -492,27 +565,6 @@ def gpu_smi_id(local: int) -> str:
         return u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         return str(local)
-
-
-def shared_schedule_split(args, plan, reps):
-    """Time the one-off expansion and one consumer layer separately."""
-    import torch
-    n = 200
-    rep = reps[0]
-    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    for _ in range(5):
-        rep[0].expand(plan)
-        rep[1].run(plan, expansion_ready=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(n):
-        rep[0].expand(plan)
-    e1.record()
-    for i in range(n):
-        reps[i % len(reps)][1 + i % (len(rep) - 1)].run(plan, expansion_ready=True)
-    e2.record()
-    torch.cuda.synchronize()
-    return {"expansion_ms": e0.elapsed_time(e1) / n, "per_layer_ms": e1.elapsed_time(e2) / n}
 
 
 def run_e2e(args, plan, inp, cols, dist, device):
@@ -637,33 +689,44 @@ def run_e2e(args, plan, inp, cols, dist, device):
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
 
 
-def _oracle_step(inp, rows, threads):
+def _oracle_step(inp, rows, threads, contig=None):
     import oracle
-    res = oracle.reference_rows(inp, rows=rows, mode="sparse", threads=threads)
+    res = oracle.reference_rows(inp, rows=rows, mode="sparse", threads=threads, contig=contig)
     return sum(int(r.end) for r in res.values())
 
 
-def run_cpu_baseline(args, inp, rank, min_seconds: float = 2.0):
-    """The oracle (candidate-only scoring + top-k) on every host core, over
-    whole passes of the batch until at least min_seconds of wall time."""
+def _oracle_contig(inp):
+    """The gathered K workspace of a prefill chunk (the oracle's gather), or None for decode rows."""
+    if hasattr(inp, "row_ke"):
+        return None
+    import oracle
+    return oracle.gather_reference(inp)
+
+
+def run_cpu_baseline(inp, workload, min_seconds=2.0):
+    """The oracle as it stands (candidate-only scoring + top-k, proven equal to the
+    dense definition by its pins) on every host core, over consecutive slices of
+    the workload's rows until min_seconds of wall time. For a prefill chunk the
+    oracle's gather runs first, untimed."""
     if isinstance(inp, list):
         inp = inp[0]
-    if not hasattr(inp, "row_ke"):
-        return None  # prefill needs the gathered workspace; reported for decode workloads
     threads = os.cpu_count() or 1
-    rows = list(range(inp.rows))
-    done_cols = 0
-    passes = 0
+    contig = _oracle_contig(inp)
+    chunk = min(inp.rows, max(4 * threads, 64))
+    done_cols = done_rows = 0
+    i = 0
     t0 = time.perf_counter()
     while True:
-        done_cols += _oracle_step(inp, rows, threads)
-        passes += 1
+        rows = [(i + j) % inp.rows for j in range(chunk)]
+        i += chunk
+        done_cols += _oracle_step(inp, rows, threads, contig)
+        done_rows += len(rows)
         if time.perf_counter() - t0 >= min_seconds:
             break
     dt = time.perf_counter() - t0
     return {"value": done_cols / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{passes} pass(es) over all {inp.rows} rows of the batch, candidate-only mode + top-k, "
-                      f"{threads} threads, {dt:.1f} s"}
+            "sample": f"{done_rows} rows of the {workload} workload ({inp.rows} per step), candidate-only mode + "
+                      f"top-k, {threads} threads, {dt:.1f} s" + ("; the K gather untimed" if contig else "")}
 
 
 def run_reference(args, rank, world):
@@ -673,26 +736,24 @@ def run_reference(args, rank, world):
     inp = make_inputs(args.workload, 0)
     if isinstance(inp, list):
         inp = inp[0]
-    if not hasattr(inp, "row_ke"):
-        return {"impl": "reference", "unavailable": "the oracle reference arm covers the decode workloads"}
     threads = os.cpu_count() or 1
+    contig = _oracle_contig(inp)
     t0 = time.perf_counter()
-    _oracle_step(inp, [0], 1)
+    _oracle_step(inp, [0], 1, contig)
     per_row = max(time.perf_counter() - t0, 1e-4)
     budget = 60.0
     rows_per_step = int(max(1, min(inp.rows, budget * threads / per_row / max(1, args.steps + args.warmup))))
-    order = list(range(inp.rows))
 
     def rows_for(i):
         s = (i * rows_per_step) % inp.rows
-        return [order[(s + j) % inp.rows] for j in range(rows_per_step)]
+        return [(s + j) % inp.rows for j in range(rows_per_step)]
 
     for i in range(args.warmup):
-        _oracle_step(inp, rows_for(i), threads)
+        _oracle_step(inp, rows_for(i), threads, contig)
     t0 = time.perf_counter()
     cols = 0
     for i in range(args.steps):
-        cols += _oracle_step(inp, rows_for(args.warmup + i), threads)
+        cols += _oracle_step(inp, rows_for(args.warmup + i), threads, contig)
     dt = time.perf_counter() - t0
     value = cols / dt
     return {
@@ -702,7 +763,8 @@ def run_reference(args, rank, world):
         "config": {"workload": args.workload, "rows_per_step": rows_per_step},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{rows_per_step} row(s) of the batch per step, candidate-only mode + top-k"},
+                         "sample": f"{rows_per_step} row(s) of the batch per step, candidate-only mode + top-k"
+                                   + ("; the K gather done once, untimed" if contig else "")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -713,15 +775,17 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
-                    choices=["decode_batch", "long_context_decode", "prefill_chunk", "prefill_chunk_paged",
-                             "shared_schedule"])
+                    choices=["tiny_decode", "decode_batch", "long_context_decode", "prefill_chunk",
+                             "prefill_chunk_paged", "shared_schedule"])
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=2.0, help="oracle time of the headline's CPU baseline")
+    ap.add_argument("--no-workloads", action="store_true", help="time the named workload only")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
