@@ -20,6 +20,10 @@ Parity status of each function (the pins live in ``tests/test_oracle_pins.py``):
   - gather: numpy slicing of the page bytes.
   - dense-then-masked == candidate-only: an invariant checked on every small
     workload.
+  - producers (K-cache writer, query quantiser): E2M1 / E4M3 / bf16 encoders
+    against the value tables' midpoints and torch's float8_e4m3fn / bfloat16
+    casts; hand-worked scale exponents; nearest-grid-point brute force; the
+    page layout through the oracle's own decode path.
 """
 
 from __future__ import annotations
@@ -41,6 +45,8 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_i64p = ctypes.POINTER(ctypes.c_int64)
 
 
 def build(out_path: str = DEFAULT_LIB, source: str = SOURCE, defines: Iterable[str] = ()) -> str:
@@ -90,6 +96,19 @@ class Oracle:
         lib.smq_oracle_expand.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int64, ctypes.c_int,
             _i32p, _i32p]
+        lib.smq_oracle_encode_e2m1.restype = ctypes.c_uint8
+        lib.smq_oracle_encode_e2m1.argtypes = [ctypes.c_double]
+        lib.smq_oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.smq_oracle_encode_e4m3.argtypes = [ctypes.c_double]
+        lib.smq_oracle_encode_bf16.restype = ctypes.c_uint16
+        lib.smq_oracle_encode_bf16.argtypes = [ctypes.c_float]
+        lib.smq_oracle_quantize_k_token.restype = ctypes.c_int
+        lib.smq_oracle_quantize_k_token.argtypes = [ctypes.c_int, _u16p, _u8p, _u8p]
+        lib.smq_oracle_write_k_cache.restype = ctypes.c_int
+        lib.smq_oracle_write_k_cache.argtypes = [ctypes.c_int, ctypes.c_int, _u16p, _i64p, ctypes.c_int64, _u8p,
+                                                 ctypes.c_int64]
+        lib.smq_oracle_quantize_q.restype = ctypes.c_int
+        lib.smq_oracle_quantize_q.argtypes = [ctypes.c_int, ctypes.c_int, _u16p, _f32p, _u8p, _f32p, _u16p]
         lib.smq_oracle_gather.restype = ctypes.c_int
         lib.smq_oracle_gather.argtypes = [
             ctypes.c_int, ctypes.c_int, _u8p, ctypes.c_int64, _i32p, ctypes.c_int64,
@@ -108,6 +127,53 @@ class Oracle:
 
     def bf16(self, bits: int) -> float:
         return self.lib.smq_oracle_bf16(bits)
+
+    # -- element encoders and producers ------------------------------------
+    def encode_e2m1(self, v: float) -> int:
+        return self.lib.smq_oracle_encode_e2m1(v)
+
+    def encode_e4m3(self, v: float) -> int:
+        return self.lib.smq_oracle_encode_e4m3(v)
+
+    def encode_bf16(self, f: float) -> int:
+        return self.lib.smq_oracle_encode_bf16(f)
+
+    def quantize_k_token(self, k_bf16: np.ndarray):
+        """One key [D] (bf16 bits) -> (packed E2M1 values [D/2], UE8M0 scales [D/32])."""
+        k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+        d = k.shape[0]
+        vals = np.empty(d // 2, dtype=np.uint8)
+        scl = np.empty(d // 32, dtype=np.uint8)
+        if self.lib.smq_oracle_quantize_k_token(d, _ptr(k, _u16p), _ptr(vals, _u8p), _ptr(scl, _u8p)) != 0:
+            raise ValueError("oracle: non-finite key")
+        return vals, scl
+
+    def write_k_cache(self, k_bf16: np.ndarray, slot_mapping: np.ndarray, cache: np.ndarray, page_size: int):
+        """Quantise keys [ntok, D] (bf16 bits) into the paged cache in place, token t to slot
+        slot_mapping[t] (page * page_size + offset; negative: skipped)."""
+        k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        assert cache.flags["C_CONTIGUOUS"] and cache.dtype == np.uint8
+        rc = self.lib.smq_oracle_write_k_cache(k.shape[1], page_size, _ptr(k, _u16p), _ptr(slots, _i64p),
+                                               k.shape[0], _ptr(cache, _u8p), cache.shape[0])
+        if rc != 0:
+            raise ValueError("oracle: slot past the cache or a non-finite key")
+
+    def quantize_q(self, q_bf16: np.ndarray, w: np.ndarray):
+        """Query rows [R, H, D] (bf16 bits) and weights [R, H] float32 -> (E4M3 codes [R, H, D],
+        float32 scales [R], bf16 weights [R, H])."""
+        q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        R, H, D = q.shape
+        q8 = np.empty((R, H, D), dtype=np.uint8)
+        sc = np.empty(R, dtype=np.float32)
+        wb = np.empty((R, H), dtype=np.uint16)
+        for r in range(R):
+            rc = self.lib.smq_oracle_quantize_q(H, D, _ptr(q[r], _u16p), _ptr(w[r], _f32p), _ptr(q8[r], _u8p),
+                                                _ptr(sc[r:], _f32p), _ptr(wb[r], _u16p))
+            if rc != 0:
+                raise ValueError(f"oracle: non-finite query or weight in row {r}")
+        return q8, sc, wb
 
     # -- per-row primitives -------------------------------------------------
     def logits_paged(self, inp, r: int, p0: int, p1: int) -> np.ndarray:

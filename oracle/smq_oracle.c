@@ -331,3 +331,131 @@ int smq_oracle_gather(int D, int page_size, const uint8_t *k_cache,
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Producers: the MXFP4 K-cache writer and the FP8 query quantiser
+ * ------------------------------------------------------------------------- */
+
+/* The model writes the MXFP4 indexer K cache, and a fused query kernel emits
+ * the FP8 query, its per-row scale and the bf16 head weights
+ * ("sparse_mqa_indexer" docs, SparseMQAIndexer and weights_dtype;
+ * "sparse_indexer.py", builder __init__: MXFP4 with UE8M0-packed
+ * granularity-32 scales). The pages give no rounding rules; the readings
+ * taken here are:
+ *  - K: per group of 32, the scale exponent e is the smallest integer with
+ *    amax <= 6 * 2^e (no element saturates), the UE8M0 code e + 127 clamped
+ *    to [1, 254]; each element x * 2^-e rounds to the nearest E2M1 value,
+ *    ties to the even code, clamped to +-6. A group of zeros has code 127.
+ *  - Q: scale = amax / 448 in float (1 for a zero row); each element
+ *    x / scale, divided in float, rounds to the nearest E4M3 value, ties to
+ *    the even code, clamped to +-448.
+ *  - weights: float to bfloat16, round to nearest, ties to even.
+ * The sign of an element that rounds to zero is kept (IEEE rounding). */
+
+/* Nearest value of a table of non-negative values (codes 0..n-1 in
+ * increasing order), ties to the even code, saturating at the last. */
+static int nearest_code(double a, const double *table, int n) {
+  if (a > table[n - 1]) a = table[n - 1]; /* saturation */
+  int best = 0;
+  for (int c = 1; c < n; ++c) {
+    double dc = fabs(a - table[c]), db = fabs(a - table[best]);
+    if (dc < db || (dc == db && (c % 2) == 0)) best = c;
+  }
+  return best;
+}
+
+uint8_t smq_oracle_encode_e2m1(double v) {
+  double table[8];
+  for (int c = 0; c < 8; ++c) table[c] = smq_oracle_e2m1((uint8_t)c);
+  int c = nearest_code(fabs(v), table, 8);
+  return (uint8_t)(signbit(v) ? (c | 8) : c);
+}
+
+uint8_t smq_oracle_encode_e4m3(double v) {
+  double table[127]; /* codes 0x00..0x7E; 0x7F is NaN */
+  for (int c = 0; c < 127; ++c) table[c] = smq_oracle_e4m3((uint8_t)c);
+  int c = nearest_code(fabs(v), table, 127);
+  return (uint8_t)(signbit(v) ? (c | 0x80) : c);
+}
+
+uint16_t smq_oracle_encode_bf16(float f) {
+  /* the bfloat16 nearest to f: compare the two neighbours that truncation
+   * and truncation plus one ulp give (f finite) */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint16_t lo = (uint16_t)(u >> 16), hi = (uint16_t)(lo + 1);
+  double dlo = fabs((double)f - smq_oracle_bf16(lo));
+  double dhi = fabs((double)f - smq_oracle_bf16(hi));
+  if (dhi < dlo || (dhi == dlo && (hi & 1) == 0)) return hi;
+  return lo;
+}
+
+/* One token's key (D bf16 values) to its packed E2M1 values [D/2] and
+ * UE8M0 scales [D/32]. */
+int smq_oracle_quantize_k_token(int D, const uint16_t *k, uint8_t *values, uint8_t *scales) {
+  for (int g = 0; g < D / 32; ++g) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double x = smq_oracle_bf16(k[32 * g + i]);
+      if (!isfinite(x)) return -1;
+      if (fabs(x) > amax) amax = fabs(x);
+    }
+    int e = 0;
+    if (amax > 0.0) {
+      e = ilogb(amax) - 3; /* 6 * 2^e < amax here; step up to the first e that covers it */
+      while (6.0 * ldexp(1.0, e) < amax) ++e;
+    }
+    int code = e + 127;
+    if (code < 1) code = 1;
+    if (code > 254) code = 254;
+    e = code - 127;
+    scales[g] = (uint8_t)code;
+    for (int i = 0; i < 32; i += 2) {
+      uint8_t lo = smq_oracle_encode_e2m1(ldexp(smq_oracle_bf16(k[32 * g + i]), -e));
+      uint8_t hi = smq_oracle_encode_e2m1(ldexp(smq_oracle_bf16(k[32 * g + i + 1]), -e));
+      values[(32 * g + i) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+  return 0;
+}
+
+/* Quantise ntok tokens' keys [ntok][D] into the paged cache: token t goes to
+ * slot slot_mapping[t] = page * page_size + offset (negative: skipped). */
+int smq_oracle_write_k_cache(int D, int page_size, const uint16_t *k, const int64_t *slot_mapping, int64_t ntok,
+                             uint8_t *cache, int64_t num_pages) {
+  int64_t page_bytes = (int64_t)page_size * (D / 2 + D / 32);
+  for (int64_t t = 0; t < ntok; ++t) {
+    int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    int64_t page = s / page_size, off = s % page_size;
+    if (page >= num_pages) return -1;
+    uint8_t *base = cache + page * page_bytes;
+    if (smq_oracle_quantize_k_token(D, k + t * D, base + off * (D / 2),
+                                    base + (int64_t)page_size * (D / 2) + off * (D / 32)) != 0)
+      return -1;
+  }
+  return 0;
+}
+
+/* One query row: q [H*D] bf16 and weights [H] float to the E4M3 codes
+ * [H*D], the float scale and the bf16 weights [H]. */
+int smq_oracle_quantize_q(int H, int D, const uint16_t *q, const float *w, uint8_t *q8, float *scale,
+                          uint16_t *w_bf16) {
+  float amax = 0.0f;
+  for (int i = 0; i < H * D; ++i) {
+    float x = (float)smq_oracle_bf16(q[i]);
+    if (!isfinite(x)) return -1;
+    if (fabsf(x) > amax) amax = fabsf(x);
+  }
+  float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  *scale = s;
+  for (int i = 0; i < H * D; ++i) {
+    float v = (float)smq_oracle_bf16(q[i]) / s;
+    q8[i] = smq_oracle_encode_e4m3((double)v);
+  }
+  for (int h = 0; h < H; ++h) {
+    if (!isfinite(w[h])) return -1;
+    w_bf16[h] = smq_oracle_encode_bf16(w[h]);
+  }
+  return 0;
+}

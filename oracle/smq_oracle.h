@@ -90,6 +90,23 @@ int smq_oracle_gather(int D, int page_size, const uint8_t *k_cache,
                       int64_t bt_cols, int64_t seq_len, uint8_t *values_out,
                       uint8_t *scales_out);
 
+/* Producers (the pages fix the formats, not the rounding; the readings are
+ * in smq_oracle.c):
+ *  - element encoders: nearest value, ties to the even code, saturating
+ *    (E2M1 at 6, E4M3 at 448); bfloat16 round to nearest even;
+ *  - one token's key [D] bf16 -> packed E2M1 values [D/2], UE8M0 scales [D/32];
+ *  - ntok keys into the paged cache through slot_mapping (negative: skipped);
+ *  - one query row [H*D] bf16 + weights [H] float -> E4M3 codes, float
+ *    scale, bf16 weights. */
+uint8_t smq_oracle_encode_e2m1(double v);
+uint8_t smq_oracle_encode_e4m3(double v);
+uint16_t smq_oracle_encode_bf16(float f);
+int smq_oracle_quantize_k_token(int D, const uint16_t *k, uint8_t *values, uint8_t *scales);
+int smq_oracle_write_k_cache(int D, int page_size, const uint16_t *k, const int64_t *slot_mapping, int64_t ntok,
+                             uint8_t *cache, int64_t num_pages);
+int smq_oracle_quantize_q(int H, int D, const uint16_t *q, const float *w, uint8_t *q8, float *scale,
+                          uint16_t *w_bf16);
+
 #ifdef __cplusplus
 }
 #endif

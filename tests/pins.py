@@ -21,6 +21,19 @@ What pins what:
   expansion_golden         hand-derived cases in golden/expansion_cases.json
   gather                   numpy slicing of the page bytes
   dense_equals_sparse      the invariant "candidate-only == dense-then-mask"
+  encoders                 E2M1: the OCP table's values and midpoints (ties to
+                           the even code), saturation; E4M3 and bf16 against
+                           torch's float8_e4m3fn / bfloat16 casts (nearest even)
+  k_scale_cases            hand-worked scale exponents: amax at and past
+                           6 * 2^e, zeros, the clamp at the smallest code
+  k_nearest                brute force: each decoded element is the nearest
+                           point of its group's grid, the exponent is the
+                           smallest that covers the group's amax
+  k_cache_layout           numpy slicing: each token's bytes sit at its slot's
+                           page and offset; other bytes stay untouched; a
+                           one-hot query reads the written keys back
+  q_quantiser              torch: scale = amax / 448 in float32, codes of
+                           x / scale cast to float8_e4m3fn, bf16 weights
 """
 
 from __future__ import annotations
@@ -349,8 +362,141 @@ def pin_dense_equals_sparse(orc):
         assert np.array_equal(d.topk, s.topk), f"row {r}: top-k"
 
 
+# -------------------------------------------------------------- producers
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def pin_encoders(orc):
+    for c in range(16):  # every table value to its own code (zero keeps its sign)
+        v = -0.0 if c == 8 else _e2m1(c)
+        assert orc.encode_e2m1(v) == c, f"e2m1 encode of {v}: {orc.encode_e2m1(v)} != {c}"
+    for i in range(7):  # midpoints to the even code of the two neighbours
+        mid = (E2M1_TABLE[i] + E2M1_TABLE[i + 1]) / 2
+        want = i if i % 2 == 0 else i + 1
+        assert orc.encode_e2m1(mid) == want, f"e2m1 midpoint {mid}"
+        assert orc.encode_e2m1(-mid) == want | 8, f"e2m1 midpoint {-mid}"
+        assert orc.encode_e2m1(mid * 0.999) == i and orc.encode_e2m1(mid * 1.001) == i + 1
+    assert orc.encode_e2m1(6.5) == 7 and orc.encode_e2m1(1e30) == 7 and orc.encode_e2m1(-7.0) == 15
+    # E4M3 against torch: every finite value, every midpoint between neighbours, random values
+    vals = torch.arange(127, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.Generator(np.random.PCG64(17))
+    xs = np.concatenate([vals, -vals, mids, -mids, rng.uniform(-450, 450, 3000), rng.normal(0, 1, 3000)])
+    xs = xs.astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(xs.tolist(), ref.tolist()):
+        assert orc.encode_e4m3(x) == r, f"e4m3 encode of {x!r}: {orc.encode_e4m3(x):#x} != {r:#x}"
+    assert orc.encode_e4m3(1e6) == 0x7E and orc.encode_e4m3(-1e6) == 0xFE
+    # bf16 against torch: ties between neighbours and random floats
+    fs = np.concatenate([1.0 + np.arange(1, 64) * 2.0 ** -8, rng.normal(0, 3, 4000)]).astype(np.float32)
+    ref = _bf16_bits(fs)
+    for f, r in zip(fs.tolist(), ref.tolist()):
+        assert orc.encode_bf16(f) == r, f"bf16 encode of {f!r}"
+
+
+def _token(values):
+    k = np.zeros(128, dtype=np.float32)
+    k[:len(values)] = values
+    return _bf16_bits(k)
+
+
+def pin_k_scale_cases(orc):
+    # (group 0's values, expected UE8M0 code): the smallest e with amax <= 6 * 2^e
+    cases = [([6.0], 127), ([6.03125], 128), ([-3.0], 126), ([3.015625, 1.0], 127), ([0.75], 124),
+             ([12.0], 128), ([12.0625], 129), ([1.0], 125), ([2.0 ** -130], 1), ([0.0], 127)]
+    for vals, code in cases:
+        v, sc = orc.quantize_k_token(_token(vals))
+        assert sc[0] == code, f"scale of amax {max(abs(x) for x in vals)}: {sc[0]} != {code}"
+        assert sc[1:].tolist() == [127, 127, 127], "groups of zeros take code 127"
+    v, sc = orc.quantize_k_token(_token([6.0, -3.0, 0.25, 0.75]))  # scale 1: codes 7, 13 (-3), 0, 2
+    assert v[0] == (7 | (13 << 4)) and v[1] == (0 | (2 << 4)), f"packed codes {v[:2]}"
+    v, sc = orc.quantize_k_token(_token([0.0] * 32 + [-0.5]))  # group 1, element 32: low nibble of byte 16
+    assert v[16] == 14 and sc[1] == 124, f"group 1 element {v[16]}, scale {sc[1]}"  # -0.5 = -4 * 2^-3
+
+
+def pin_k_nearest(orc):
+    rng = np.random.Generator(np.random.PCG64(23))
+    grid = np.array(sorted({s * t for t in E2M1_TABLE for s in (-1.0, 1.0)}))
+    for trial in range(40):
+        scale = 2.0 ** rng.integers(-20, 20)
+        x = (rng.standard_normal(128) * scale * (1 + 3 * (trial % 3))).astype(np.float32)
+        kb = _bf16_bits(x)
+        xv = torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+        v, sc = orc.quantize_k_token(kb)
+        for g in range(4):
+            e = int(sc[g]) - 127
+            seg = xv[32 * g:32 * g + 32]
+            amax = np.abs(seg).max()
+            assert amax <= 6 * 2.0 ** e and (amax > 6 * 2.0 ** (e - 1) or sc[g] == 1), f"group {g} exponent"
+            for i in range(32):
+                d = 32 * g + i
+                code = (v[d // 2] >> (4 * (d % 2))) & 15
+                got = _e2m1(code) * 2.0 ** e
+                best = np.abs(grid * 2.0 ** e - seg[i]).min()
+                assert abs(got - seg[i]) == best, f"element {d}: {got} is not a nearest grid point of {seg[i]}"
+
+
+def pin_k_cache_layout(orc):
+    rng = np.random.Generator(np.random.PCG64(29))
+    page, npages, ntok = 16, 6, 40
+    pb = page * 68
+    k = _bf16_bits(rng.standard_normal((ntok, 128)).astype(np.float32))
+    slots = rng.permutation(page * npages)[:ntok].astype(np.int64)
+    slots[::7] = -1
+    cache = np.full((npages, pb), 0xA5, dtype=np.uint8)
+    orc.write_k_cache(k, slots, cache, page)
+    expect = np.full((npages, pb), 0xA5, dtype=np.uint8)
+    for t in range(ntok):
+        if slots[t] < 0:
+            continue
+        pg, off = divmod(int(slots[t]), page)
+        v, sc = orc.quantize_k_token(k[t])
+        expect[pg, off * 64:(off + 1) * 64] = v
+        expect[pg, page * 64 + off * 4:page * 64 + (off + 1) * 4] = sc
+    assert np.array_equal(cache, expect), "written page bytes"
+    # read back through the decode path: a one-hot query at d* gives max(0, K[t, d*])
+    g = synth.Geometry(8, 128, page, 16, 1, 1)
+    bt = np.arange(npages, dtype=np.int32)[None, :]
+    for d in (0, 33, 127):
+        q8 = np.zeros((1, 8, 128), dtype=np.uint8)
+        q8[0, 0, d] = E4M3_ONE
+        w = np.zeros((1, 8), dtype=np.uint16)
+        w[0, 0] = BF16_ONE
+        inp = synth.DecodeInputs(g, q8, np.array([1.0], dtype=np.float32), w, cache, bt,
+                                 np.zeros(1, dtype=np.int32), np.array([page * npages], dtype=np.int32),
+                                 np.zeros((1, 1), dtype=np.int32))
+        logits = orc.logits_paged(inp, 0, 0, page * npages)
+        for t in range(ntok):
+            if slots[t] < 0:
+                continue
+            v, sc = orc.quantize_k_token(k[t])
+            kd = _e2m1((v[d // 2] >> (4 * (d % 2))) & 15) * 2.0 ** (int(sc[d // 32]) - 127)
+            assert abs(logits[slots[t]] - max(0.0, kd)) <= 1e-12 * max(1.0, abs(kd)), f"token {t} d {d}"
+
+
+def pin_q_quantiser(orc):
+    rng = np.random.Generator(np.random.PCG64(31))
+    R, H = 5, 16
+    x = rng.standard_normal((R, H, 128)).astype(np.float32) * np.array([1, 1e-3, 40, 1, 2], dtype=np.float32)[:, None, None]
+    x[3] = 0.0  # a zero row: scale 1
+    qb = _bf16_bits(x)
+    w = rng.standard_normal((R, H)).astype(np.float32)
+    q8, sc, wb = orc.quantize_q(qb, w)
+    xt = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).to(torch.float32)
+    amax = xt.abs().reshape(R, -1).amax(dim=1)
+    st = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert np.array_equal(sc, st.numpy()), "per-row scale amax / 448"
+    ref = (xt / st[:, None, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q8, ref), "E4M3 codes of x / scale"
+    assert np.array_equal(wb, _bf16_bits(w)), "bf16 weights"
+
+
 ALL_PINS = [
     pin_e4m3, pin_bf16, pin_e2m1, pin_ue8m0, pin_one_hot, pin_relu_sign, pin_exact_rational,
     pin_numpy_einsum, pin_monotone_topk, pin_ties, pin_padding, pin_expansion_golden, pin_gather,
-    pin_dense_equals_sparse,
+    pin_dense_equals_sparse, pin_encoders, pin_k_scale_cases, pin_k_nearest, pin_k_cache_layout, pin_q_quantiser,
 ]

@@ -46,6 +46,20 @@ MUTANTS = {
     "expansion keeps repeats": ("if (nu == 0 || kept[nu - 1] != kept[i]) kept[nu++] = kept[i];",
                                 "kept[nu++] = kept[i];"),
     "expansion end rounds up": ("cols += (L - start < sbkv) ? (L - start) : sbkv;", "cols += sbkv;"),
+    "encode ties to odd": ("if (dc < db || (dc == db && (c % 2) == 0)) best = c;",
+                           "if (dc < db || (dc == db && (c % 2) == 1)) best = c;"),
+    "encode without saturation": ("if (a > table[n - 1]) a = table[n - 1]; /* saturation */", "/* no saturation */"),
+    "k scale against 4": ("while (6.0 * ldexp(1.0, e) < amax) ++e;", "while (4.0 * ldexp(1.0, e) < amax) ++e;"),
+    "k scale clamp": ("if (code < 1) code = 1;", "if (code < 0) code = 0;"),
+    "k nibbles swapped": ("values[(32 * g + i) / 2] = (uint8_t)(lo | (hi << 4));",
+                          "values[(32 * g + i) / 2] = (uint8_t)(hi | (lo << 4));"),
+    "k slot offset": ("int64_t page = s / page_size, off = s % page_size;",
+                      "int64_t page = s / page_size, off = (s + 1) % page_size;"),
+    "k scales placement": ("base + (int64_t)page_size * (D / 2) + off * (D / 32)) != 0)",
+                           "base + (int64_t)page_size * (D / 2) + (off ^ 1) * (D / 32)) != 0)"),
+    "q scale 447": ("float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
+    "q zero-row scale": ("float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 448.0f : 0.5f;"),
+    "bf16 ties down": ("if (dhi < dlo || (dhi == dlo && (hi & 1) == 0)) return hi;", "if (dhi < dlo) return hi;"),
     "gather scale offset": ("base + (int64_t)page_size * (D / 2) + tok * (D / 32),\n           (size_t)(D / 32));",
                             "base + (int64_t)page_size * (D / 2),\n           (size_t)(D / 32));"),
 }
