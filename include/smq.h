@@ -286,6 +286,47 @@ SMQ_API int sparse_mqa_gather_k(const smq_plan *plan, const uint8_t *k_cache, in
                                 uint8_t *k_values, uint8_t *k_scales, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* Producers of the indexer's inputs. (Source: sparse_mqa_indexer docs,
+ * SparseMQAIndexer and weights_dtype: the model writes the MXFP4 indexer K
+ * cache, and a fused query kernel writes the FP8 query, its scale and the
+ * bf16 weights; sparse_indexer.py, builder __init__: MXFP4 with UE8M0-packed
+ * granularity-32 scales.) The pages fix the formats but not the rounding.
+ * This library's rounding:
+ *  - K, per group of 32 elements: the scale exponent e is the smallest
+ *    integer with amax <= 6 * 2^e, stored as the UE8M0 code e + 127 clamped
+ *    to [1, 254] (a group of zeros: 127). Each element x * 2^-e rounds to the
+ *    nearest E2M1 value, ties to even, saturating at 6.
+ *  - Q, per row: scale = amax / 448 (1 for a row of zeros). Each element
+ *    x / scale (float division) rounds to the nearest E4M3 value, ties to
+ *    even, saturating at 448.
+ *  - weights: float to the nearest-even bfloat16.
+ * The sign of an element that rounds to zero is kept. Inputs must be finite.
+ * RoPE, which the pages' fused query kernel also applies, is not defined on
+ * the pages and is not part of this call. */
+
+/* Write ntok keys into the paged K cache (layout at the top of this file).
+ *  - k: device [ntok][D] bfloat16 bits, 16-byte aligned.
+ *  - slot_mapping: device [ntok] int64. Token t goes to page
+ *    slot_mapping[t] / page_size, row slot_mapping[t] % page_size; a negative
+ *    slot skips the token.
+ *  - k_cache: device [num_pages][page_bytes], 16-byte aligned.
+ * A slot past the cache raises SMQ_ERR_BOUNDS in the workspace status word
+ * (at least smq_workspace_size(plan, 0) bytes), and that token is skipped.
+ * Tokens that share a slot race. ntok may be 0. */
+SMQ_API int sparse_mqa_write_k_cache(const smq_plan *plan, const uint16_t *k, const int64_t *slot_mapping,
+                                     int64_t ntok, uint8_t *k_cache, int64_t num_pages, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* Quantise `rows` query rows and their head weights.
+ *  - q: device [rows][H][D] bfloat16 bits, 16-byte aligned.
+ *  - weights: device [rows][H] float.
+ *  - q_fp8: device [rows][H][D] E4M3 out, 16-byte aligned. q_scale: device
+ *    [rows] float out. weights_bf16: device [rows][H] bfloat16 bits out.
+ * These are the q, q_scale and weights of the decode and prefill calls.
+ * rows may be 0. */
+SMQ_API int sparse_mqa_quantize_q(const smq_plan *plan, const uint16_t *q, const float *weights, int32_t rows,
+                                  uint8_t *q_fp8, float *q_scale, uint16_t *weights_bf16, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

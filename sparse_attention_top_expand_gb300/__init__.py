@@ -68,6 +68,7 @@ EXPORTED = [
     "smq_plan_create", "smq_plan_destroy", "smq_plan_get_info", "smq_workspace_size", "smq_workspace_init",
     "smq_get_status", "smq_error_string", "sparse_mqa_candidate_expand", "sparse_mqa_logits_topk_decode",
     "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k", "sparse_mqa_logits_topk_decode_noalloc",
+    "sparse_mqa_write_k_cache", "sparse_mqa_quantize_q",
 ]
 
 _lib = None
@@ -96,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_mqa_logits_topk_prefill_chunk.argtypes = [_vp, P(SMQPrefillArgs), _vp]
     lib.sparse_mqa_gather_k.argtypes = [_vp, _vp, _c_i64, _vp, _c_i32, _vp, _c_i32, _c_i64, _vp, _vp, _vp,
                                         ctypes.c_size_t, _vp]
+    lib.sparse_mqa_write_k_cache.argtypes = [_vp, _vp, _vp, _c_i64, _vp, _c_i64, _vp, ctypes.c_size_t, _vp]
+    lib.sparse_mqa_quantize_q.argtypes = [_vp, _vp, _vp, _c_i32, _vp, _vp, _vp, _vp]
     for name in EXPORTED:
         if name != "smq_error_string":
             getattr(lib, name).restype = ctypes.c_int
@@ -371,3 +374,22 @@ def sparse_mqa_gather_k(plan: Plan, k_cache, block_table, cu_seq_lens, total_len
         _ptr(cu_seq_lens, _I32, "cu_seq_lens", dev), int(cu_seq_lens.shape[0]) - 1, int(total_len),
         _ptr(k_values, _U8, "k_values", dev), _ptr(k_scales, _U8, "k_scales", dev),
         _ptr(workspace, _U8, "workspace", dev), workspace.numel(), _stream(stream)), "sparse_mqa_gather_k")
+
+
+def sparse_mqa_write_k_cache(plan: Plan, k, slot_mapping, k_cache, workspace, stream=None) -> None:
+    """Quantise keys [ntok, D] (bf16) into the paged MXFP4 cache at slot_mapping [ntok] (int64)."""
+    dev = plan.device
+    _check(load_library().sparse_mqa_write_k_cache(
+        plan.handle, _ptr(k, _BF16, "k", dev), _ptr(slot_mapping, (torch.int64,), "slot_mapping", dev),
+        int(k.shape[0]), _ptr(k_cache, _U8, "k_cache", dev), int(k_cache.shape[0]),
+        _ptr(workspace, _U8, "workspace", dev), workspace.numel(), _stream(stream)), "sparse_mqa_write_k_cache")
+
+
+def sparse_mqa_quantize_q(plan: Plan, q, weights, q_fp8, q_scale, weights_bf16, stream=None) -> None:
+    """Quantise query rows [R, H, D] (bf16) to E4M3 with a float scale per row, and float
+    weights [R, H] to bf16."""
+    dev = plan.device
+    _check(load_library().sparse_mqa_quantize_q(
+        plan.handle, _ptr(q, _BF16, "q", dev), _ptr(weights, _F32, "weights", dev), int(q.shape[0]),
+        _ptr(q_fp8, _U8, "q_fp8", dev), _ptr(q_scale, _F32, "q_scale", dev),
+        _ptr(weights_bf16, _BF16, "weights_bf16", dev), _stream(stream)), "sparse_mqa_quantize_q")

@@ -1,6 +1,6 @@
 """Build libsmq.so, the sm_103a C-ABI library, in-tree with nvcc.
 
-Two translation units are compiled in parallel and then linked. Only the
+Three translation units are compiled in parallel and then linked. Only the
 SMQ_API entry points of include/smq.h are exported.
 """
 
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsmq.so")
 TRACE_LIB = os.path.join(PKG, "libsmq_trace.so")  # -DSMQ_TRACE: phase timestamps (include/smq_trace.h)
-SOURCES = ["smq_api.cu", "smq_kernels.cu"]
+SOURCES = ["smq_api.cu", "smq_kernels.cu", "smq_producers.cu"]
 HEADERS = ["smq_kernels.cuh", "smq_ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -582,6 +582,50 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const sm
   return sparse_mqa_logits_topk_decode(plan, &a, stream);
 }
 
+SMQ_API int sparse_mqa_write_k_cache(const smq_plan* plan, const uint16_t* k, const int64_t* slot_mapping,
+                                     int64_t ntok, uint8_t* k_cache, int64_t num_pages, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (!plan || ntok < 0) return SMQ_ERR_INVALID_ARG;
+  if (ntok == 0) return SMQ_OK;
+  if (!k || !slot_mapping || !k_cache || !workspace || num_pages <= 0) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(slot_mapping, 8) || !aligned(k_cache, 16) || !aligned(workspace, 16))
+    return SMQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kStatusBytes) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  int rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  smq::KWriteParams w;
+  w.k = k;
+  w.slot_mapping = slot_mapping;
+  w.ntok = ntok;
+  w.page_size = plan->desc.page_size;
+  w.num_pages = num_pages;
+  w.page_bytes = plan->page_bytes;
+  w.k_cache = k_cache;
+  w.status = static_cast<int32_t*>(workspace);
+  return smq::launch_write_k_cache(w, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
+SMQ_API int sparse_mqa_quantize_q(const smq_plan* plan, const uint16_t* q, const float* weights, int32_t rows,
+                                  uint8_t* q_fp8, float* q_scale, uint16_t* weights_bf16, void* stream) {
+  if (!plan || rows < 0) return SMQ_ERR_INVALID_ARG;
+  if (rows == 0) return SMQ_OK;
+  if (!q || !weights || !q_fp8 || !q_scale || !weights_bf16) return SMQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(q_fp8, 16) || !aligned(weights, 4) || !aligned(q_scale, 4) ||
+      !aligned(weights_bf16, 2))
+    return SMQ_ERR_INVALID_ARG;
+  int rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  smq::QQuantParams p;
+  p.q = q;
+  p.weights_in = weights;
+  p.rows = rows;
+  p.heads = plan->desc.num_heads;
+  p.q_fp8 = q_fp8;
+  p.q_scale = q_scale;
+  p.weights_out = weights_bf16;
+  return smq::launch_quantize_q(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
 #ifdef SMQ_TRACE
 SMQ_API int smq_trace_read(uint64_t* host, size_t count) {
   if (!host) return SMQ_ERR_INVALID_ARG;

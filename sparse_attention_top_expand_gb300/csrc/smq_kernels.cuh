@@ -162,6 +162,33 @@ struct GatherParams {
   int32_t* status;
 };
 
+// The MXFP4 K-cache writer: bf16 keys [ntok][128] to slots of the paged cache.
+struct KWriteParams {
+  const uint16_t* k;
+  const int64_t* slot_mapping;  // [ntok] page * page_size + offset; negative: skipped
+  int64_t ntok;
+  int32_t page_size;
+  int64_t num_pages;
+  int64_t page_bytes;
+  uint8_t* k_cache;
+  int32_t* status;  // SMQ_ERR_BOUNDS for a slot past the cache
+};
+
+// The query quantiser: bf16 rows [rows][heads][128] to E4M3 and a float
+// scale per row; float weights [rows][heads] to bf16.
+struct QQuantParams {
+  const uint16_t* q;
+  const float* weights_in;
+  int64_t rows;
+  int32_t heads;
+  uint8_t* q_fp8;
+  float* q_scale;
+  uint16_t* weights_out;
+};
+
+cudaError_t launch_write_k_cache(const KWriteParams& p, cudaStream_t stream);
+cudaError_t launch_quantize_q(const QQuantParams& p, cudaStream_t stream);
+
 // Shared-memory bytes of the score kernel for a geometry.
 size_t score_smem_bytes(int n_mma, int heads, int rows);
 
