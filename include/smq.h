@@ -203,6 +203,12 @@ typedef struct smq_decode_args {
   void *profile_events[4];        /* optional cudaEvent_t, recorded on the stream before the
                                      expansion, before the gather+score kernel, before the top-k
                                      and after it; NULL entries are skipped */
+  uint16_t *logits_out_bf16;      /* device [R][S] bf16 logits by sparse column, each the fp32
+                                     logit rounded to the nearest-even bf16 (columns >= end are
+                                     -inf), or NULL. The top-k still selects on the fp32 logits.
+                                     Read only when struct_size covers it. (Source:
+                                     sparse_indexer.py, builder __init__: DeepSelect takes bf16
+                                     logits.) */
 } smq_decode_args;
 
 SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan *plan, const smq_decode_args *args,
@@ -263,6 +269,7 @@ typedef struct smq_prefill_args {
   void *workspace;
   size_t workspace_bytes;
   void *profile_events[4];        /* as in smq_decode_args */
+  uint16_t *logits_out_bf16;      /* as in smq_decode_args */
 } smq_prefill_args;
 
 SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan *plan, const smq_prefill_args *args,

@@ -5,6 +5,11 @@ oracle is exact to ~1e-15 relative (double arithmetic over products that
 are exact in double); the GPU accumulates the same products in fp32, so any
 deviation above ~1e-5 relative means a bug, far inside the bound.
 
+bf16 logits (the optional bf16 output): each is the fp32 logit rounded to
+the nearest-even bfloat16, so a column passes when |gpu - ref| <=
+max(ATOL, RTOL * |ref|) + 2^-8 * |ref|: with 8 significant bits, half a
+bf16 step is at most 2^-8 of the value.
+
 Top-k: the output order inside a row is not specified by the pages, so rows
 are compared as sets.  The count of ids must be min(k, |valid|) and the rest
 -1; ids must be distinct valid positions; an id that one side picked and the
@@ -39,6 +44,19 @@ def check_logits(gpu: np.ndarray, ref: np.ndarray, what: str = "logits") -> None
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {len(ref)} columns out of tolerance; first at {i}: "
             f"gpu={gpu[i]!r} ref={ref[i]!r}")
+
+
+def check_logits_bf16(gpu: np.ndarray, ref: np.ndarray, what: str = "bf16 logits") -> None:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if gpu.shape != ref.shape:
+        raise AssertionError(f"{what}: shape {gpu.shape} != {ref.shape}")
+    bound = tol(ref) + np.abs(ref) * 2.0 ** -8
+    bad = ~(np.abs(gpu - ref) <= bound)
+    if bad.any():
+        i = int(np.flatnonzero(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {len(ref)} columns out of tolerance; first at {i}: "
+                             f"gpu={gpu[i]!r} ref={ref[i]!r}")
 
 
 def check_topk(gpu_ids: np.ndarray, row, k: int, what: str = "topk") -> None:

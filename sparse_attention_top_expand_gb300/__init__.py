@@ -52,7 +52,7 @@ class SMQDecodeArgs(ctypes.Structure):
                 ("bt_stride", _c_i32), ("row_indices", _vp), ("row_ke", _vp), ("candidate_blocks", _vp),
                 ("topk_out", _vp), ("topk_ld", _c_i32), ("sparse_indices", _vp), ("end", _vp),
                 ("expansion_ready", _c_i32), ("col_indices", _vp), ("logits_out", _vp), ("workspace", _vp),
-                ("workspace_bytes", ctypes.c_size_t), ("profile_events", _vp * 4)]
+                ("workspace_bytes", ctypes.c_size_t), ("profile_events", _vp * 4), ("logits_out_bf16", _vp)]
 
 
 class SMQPrefillArgs(ctypes.Structure):
@@ -61,7 +61,7 @@ class SMQPrefillArgs(ctypes.Structure):
                 ("cu_seqlen_ke", _vp), ("candidate_blocks", _vp), ("topk_out", _vp), ("topk_ld", _c_i32),
                 ("sparse_indices", _vp), ("end", _vp), ("expansion_ready", _c_i32), ("col_indices", _vp),
                 ("logits_out", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("profile_events", _vp * 4)]
+                ("profile_events", _vp * 4), ("logits_out_bf16", _vp)]
 
 
 EXPORTED = [
@@ -237,7 +237,8 @@ def sparse_mqa_candidate_expand(plan: Plan, candidate_blocks, row_ks, row_ke, sp
 
 
 def _decode_args(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
-                 topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out):
+                 topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out,
+                 logits_out_bf16=None):
     dev = plan.device
     a = SMQDecodeArgs()
     a.struct_size = ctypes.sizeof(SMQDecodeArgs)
@@ -260,17 +261,20 @@ def _decode_args(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indi
     a.expansion_ready = 1 if expansion_ready else 0
     a.col_indices = _ptr(col_indices, _I32, "col_indices", dev)
     a.logits_out = _ptr(logits_out, _F32, "logits_out", dev)
-    a.workspace = _ptr(workspace, _U8, "workspace", dev)
-    a.workspace_bytes = workspace.numel()
+    a.logits_out_bf16 = _ptr(logits_out_bf16, _BF16, "logits_out_bf16", dev)
+    if workspace is not None:
+        a.workspace = _ptr(workspace, _U8, "workspace", dev)
+        a.workspace_bytes = workspace.numel()
     return a
 
 
 def sparse_mqa_logits_topk_decode(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke,
                                   candidate_blocks, topk_out, sparse_indices, end, workspace,
                                   expansion_ready: bool = False, col_indices=None, logits_out=None,
-                                  stream=None, profile_events=None) -> None:
+                                  stream=None, profile_events=None, logits_out_bf16=None) -> None:
     a = _decode_args(plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
-                     topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out)
+                     topk_out, sparse_indices, end, workspace, expansion_ready, col_indices, logits_out,
+                     logits_out_bf16)
     _set_events(a, profile_events)
     _check(load_library().sparse_mqa_logits_topk_decode(plan.handle, ctypes.byref(a), _stream(stream)),
            "sparse_mqa_logits_topk_decode")
@@ -304,32 +308,12 @@ class DecodeCall:
 def sparse_mqa_logits_topk_decode_noalloc(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices,
                                           row_ke, candidate_blocks, topk_out, sparse_indices, end,
                                           expansion_ready: bool = False, col_indices=None, logits_out=None,
-                                          stream=None) -> None:
+                                          stream=None, logits_out_bf16=None) -> None:
     """Paged decode on the library's static scratch: no workspace argument,
     at most 8 MiB of fp32 logits (rows x sparse columns), calls must not
     overlap on the GPU, device-detected errors are not reported."""
-    dev = plan.device
-    a = SMQDecodeArgs()
-    a.struct_size = ctypes.sizeof(SMQDecodeArgs)
-    a.rows = int(q.shape[0])
-    a.q = _ptr(q, _U8, "q", dev)
-    a.q_scale = _ptr(q_scale, _F32, "q_scale", dev)
-    a.weights = _ptr(weights, _BF16, "weights", dev)
-    a.k_cache = _ptr(k_cache, _U8, "k_cache", dev)
-    a.num_pages = int(k_cache.shape[0])
-    a.block_table = _ptr(block_table, _I32, "block_table", dev)
-    a.bt_rows = int(block_table.shape[0])
-    a.bt_stride = int(block_table.shape[1])
-    a.row_indices = _ptr(row_indices, _I32, "row_indices", dev)
-    a.row_ke = _ptr(row_ke, _I32, "row_ke", dev)
-    a.candidate_blocks = _ptr(candidate_blocks, _I32, "candidate_blocks", dev)
-    a.topk_out = _ptr(topk_out, _I32, "topk_out", dev)
-    a.topk_ld = int(topk_out.shape[1])
-    a.sparse_indices = _ptr(sparse_indices, _I32, "sparse_indices", dev)
-    a.end = _ptr(end, _I32, "end", dev)
-    a.expansion_ready = 1 if expansion_ready else 0
-    a.col_indices = _ptr(col_indices, _I32, "col_indices", dev)
-    a.logits_out = _ptr(logits_out, _F32, "logits_out", dev)
+    a = _decode_args(plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke, candidate_blocks,
+                     topk_out, sparse_indices, end, None, expansion_ready, col_indices, logits_out, logits_out_bf16)
     _check(load_library().sparse_mqa_logits_topk_decode_noalloc(plan.handle, ctypes.byref(a), _stream(stream)),
            "sparse_mqa_logits_topk_decode_noalloc")
 
@@ -337,7 +321,7 @@ def sparse_mqa_logits_topk_decode_noalloc(plan: Plan, q, q_scale, weights, k_cac
 def sparse_mqa_logits_topk_prefill_chunk(plan: Plan, q, q_scale, weights, k_values, k_scales, cu_seqlen_ks,
                                          cu_seqlen_ke, candidate_blocks, topk_out, sparse_indices, end, workspace,
                                          expansion_ready: bool = False, col_indices=None, logits_out=None,
-                                         stream=None, profile_events=None) -> None:
+                                         stream=None, profile_events=None, logits_out_bf16=None) -> None:
     dev = plan.device
     a = SMQPrefillArgs()
     a.struct_size = ctypes.sizeof(SMQPrefillArgs)
@@ -358,6 +342,7 @@ def sparse_mqa_logits_topk_prefill_chunk(plan: Plan, q, q_scale, weights, k_valu
     a.expansion_ready = 1 if expansion_ready else 0
     a.col_indices = _ptr(col_indices, _I32, "col_indices", dev)
     a.logits_out = _ptr(logits_out, _F32, "logits_out", dev)
+    a.logits_out_bf16 = _ptr(logits_out_bf16, _BF16, "logits_out_bf16", dev)
     a.workspace = _ptr(workspace, _U8, "workspace", dev)
     a.workspace_bytes = workspace.numel()
     _set_events(a, profile_events)

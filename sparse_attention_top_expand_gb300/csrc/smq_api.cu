@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -126,6 +127,19 @@ void record(void* ev, cudaStream_t s) {
     cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
 }
 
+// The bf16 logits pointer of an argument struct, or null when the caller's
+// struct_size predates the field.
+template <typename A>
+uint16_t* bf16_logits(const A* a) {
+  return a->struct_size >= offsetof(A, logits_out_bf16) + sizeof(a->logits_out_bf16) ? a->logits_out_bf16 : nullptr;
+}
+
+// The smallest struct_size accepted: the struct without its last field.
+template <typename A>
+bool struct_ok(const A* a) {
+  return a->struct_size >= offsetof(A, logits_out_bf16);
+}
+
 struct CommonRows {
   int32_t rows;
   const uint8_t* q;
@@ -141,6 +155,7 @@ struct CommonRows {
   float* logits_out;
   void* workspace;
   size_t workspace_bytes;
+  uint16_t* logits_out_bf16;
 };
 
 int check_common(const smq_plan* p, const CommonRows& a) {
@@ -154,6 +169,7 @@ int check_common(const smq_plan* p, const CommonRows& a) {
       !aligned(a.topk_out, 4) || !aligned(a.sparse_indices, 4) || !aligned(a.end, 4))
     return SMQ_ERR_INVALID_ARG;
   if (a.logits_out && !aligned(a.logits_out, 4)) return SMQ_ERR_INVALID_ARG;
+  if (a.logits_out_bf16 && !aligned(a.logits_out_bf16, 2)) return SMQ_ERR_INVALID_ARG;
   if (a.workspace_bytes < workspace_bytes_for(p, a.rows)) return SMQ_ERR_WORKSPACE_TOO_SMALL;
   return SMQ_OK;
 }
@@ -175,6 +191,7 @@ smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a) {
   s.end = a.end;
   s.status = static_cast<int32_t*>(a.workspace);
   s.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes);
+  s.logits_bf16 = a.logits_out_bf16;
   s.logits = a.logits_out ? a.logits_out
                           : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes +
                                                      counter_bytes(p));
@@ -207,6 +224,7 @@ int run_topk(const smq_plan* p, const CommonRows& a, const smq::ScoreParams& s, 
   t.num_cols = p->num_cols;
   t.logits = s.logits;
   t.logits_fill = a.logits_out;
+  t.logits_fill_bf16 = a.logits_out_bf16;
   t.sparse_indices = a.sparse_indices;
   t.end = a.end;
   t.topk_out = a.topk_out;
@@ -383,10 +401,11 @@ SMQ_API int sparse_mqa_candidate_expand(const smq_plan* plan, const int32_t* can
 }
 
 SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode_args* args, void* stream) {
-  if (!plan || !args || args->struct_size < sizeof(smq_decode_args)) return SMQ_ERR_INVALID_ARG;
+  if (!plan || !args || !struct_ok(args)) return SMQ_ERR_INVALID_ARG;
   const smq_decode_args& a = *args;
   CommonRows c{a.rows, a.q, a.q_scale, a.weights, a.candidate_blocks, a.topk_out, a.topk_ld, a.sparse_indices,
-               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes};
+               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes,
+               bf16_logits(args)};
   int rc = check_common(plan, c);
   if (rc != SMQ_OK || a.rows == 0) return rc;
   if (!a.k_cache || !a.block_table || !a.row_ke || a.num_pages <= 0 || a.bt_rows <= 0 || a.bt_stride <= 0)
@@ -491,10 +510,11 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan* plan, const smq_decode
 
 SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq_prefill_args* args,
                                                  void* stream) {
-  if (!plan || !args || args->struct_size < sizeof(smq_prefill_args)) return SMQ_ERR_INVALID_ARG;
+  if (!plan || !args || !struct_ok(args)) return SMQ_ERR_INVALID_ARG;
   const smq_prefill_args& a = *args;
   CommonRows c{a.rows, a.q, a.q_scale, a.weights, a.candidate_blocks, a.topk_out, a.topk_ld, a.sparse_indices,
-               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes};
+               a.end, a.expansion_ready, a.col_indices, a.logits_out, a.workspace, a.workspace_bytes,
+               bf16_logits(args)};
   int rc = check_common(plan, c);
   if (rc != SMQ_OK || a.rows == 0) return rc;
   if (!a.k_values || !a.k_scales || !a.cu_seqlen_ks || !a.cu_seqlen_ke || a.total_len <= 0 ||
@@ -560,7 +580,7 @@ SMQ_API int sparse_mqa_gather_k(const smq_plan* plan, const uint8_t* k_cache, in
 
 SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const smq_decode_args* args,
                                                   void* stream) {
-  if (!plan || !args || args->struct_size < sizeof(smq_decode_args)) return SMQ_ERR_INVALID_ARG;
+  if (!plan || !args || !struct_ok(args)) return SMQ_ERR_INVALID_ARG;
   if (args->workspace || args->workspace_bytes) return SMQ_ERR_INVALID_ARG;  // the library's scratch replaces it
   if (args->rows < 0 || args->rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
   if (workspace_bytes_for(plan, args->rows) > kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES)
@@ -576,7 +596,10 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const sm
   if (cudaMemsetAsync(scratch, 0, kStatusBytes + counter_bytes(plan), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return SMQ_ERR_CUDA;
-  smq_decode_args a = *args;
+  smq_decode_args a;  // the caller's fields (as many as its struct_size holds), then the scratch
+  std::memset(&a, 0, sizeof a);
+  std::memcpy(&a, args, args->struct_size < sizeof a ? args->struct_size : sizeof a);
+  a.struct_size = sizeof a;
   a.workspace = scratch;
   a.workspace_bytes = kStatusBytes + SMQ_NOALLOC_SCRATCH_BYTES;
   return sparse_mqa_logits_topk_decode(plan, &a, stream);

@@ -39,6 +39,7 @@
 #include "smq_ptx.cuh"
 
 #include <cfloat>
+#include <cuda_bf16.h>
 
 namespace smq {
 
@@ -119,6 +120,10 @@ __device__ __forceinline__ int find_row(const int32_t* prefix, int rows, int64_t
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) { atomicOr(status, code); }
+
+// float to the nearest-even bfloat16 bits
+__device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+constexpr uint16_t kBf16NegInf = 0xFF80;
 
 }  // namespace
 
@@ -410,7 +415,8 @@ struct TopkScratch {
 // CTA's shared memory.
 template <int kThreads, int kJ, bool kWide, bool kShared = false>
 __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k, const int32_t* sparse_row, int nsb,
-                            int sbkv, int32_t* out, int32_t* colo, float* fill, const TopkScratch& sm) {
+                            int sbkv, int32_t* out, int32_t* colo, float* fill, uint16_t* fill16,
+                            const TopkScratch& sm) {
   constexpr int kWarps = kThreads / 32;
   constexpr int kChunks = kWarps * kJ;  // 32-column chunks of the row, chunk j * kWarps + warp
   constexpr int kPerThread = (kTopkBins + kThreads - 1) / kThreads;  // bins a thread scans
@@ -434,6 +440,8 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   for (int i = tid; i < (kWide ? kTopkBins : 256 * 32) / 4; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
   if (fill)
     for (int c = e + tid; c < S; c += kThreads) fill[c] = -INFINITY;
+  if (fill16)
+    for (int c = e + tid; c < S; c += kThreads) fill16[c] = kBf16NegInf;
   const int32_t* sidx = sm.sidx;
   const int sb_shift = 31 - __clz(sbkv);  // the sub-block size is a power of two (16..128)
   auto token = [&](int c) { return (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1)); };
@@ -700,6 +708,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         if (p.logits_fill)
           for (int c = 0; c < S; ++c) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
+        if (p.logits_bf16)
+          for (int c = 0; c < S; ++c) p.logits_bf16[static_cast<int64_t>(r) * S + c] = kBf16NegInf;
       }
     }
   }
@@ -1112,7 +1122,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
         const int col = static_cast<int>(t - prefix[r]) * kTileM + h * kMmaM + m;
-        if (col < e) p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
+        if (col < e) {
+          p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
+          if (p.logits_bf16) p.logits_bf16[static_cast<int64_t>(row) * S + col] = to_bf16(acc * qs);
+        }
       }
       if (warp == 2 && lane == 0 && ie == 0) SMQ_MARK(11);
       if (warp == 2 && lane == 0 && ie == n - 1) SMQ_MARK(12);
@@ -1393,11 +1406,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         int32_t* out = p.topk_out + static_cast<int64_t>(r) * p.topk_ld;
         int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr;
         float* fill = p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr;
+        uint16_t* fill16 = p.logits_bf16 ? p.logits_bf16 + static_cast<int64_t>(r) * S : nullptr;
         const int32_t* srow = p.sparse_indices_out + static_cast<int64_t>(r) * p.nsb;
         if (S <= kScoreThreads * 11)
-          select_topk<kScoreThreads, 11, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+          select_topk<kScoreThreads, 11, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, fill16, sm);
         else
-          select_topk<kScoreThreads, 22, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, sm);
+          select_topk<kScoreThreads, 22, true>(L, S, e_clean, p.topk, srow, p.nsb, sbkv, out, colo, fill, fill16, sm);
         __syncthreads();  // the scratch is reused by the next row
         if (tid == 0) SMQ_MARK(15);
       }
@@ -1437,7 +1451,8 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? (kJ <= 8 ? 6 : 4) 
                                 p.sparse_indices + static_cast<int64_t>(r) * p.nsb, p.nsb, p.sbkv,
                                 p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
                                 p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr,
-                                p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr, sm);
+                                p.logits_fill ? p.logits_fill + static_cast<int64_t>(r) * S : nullptr,
+                                p.logits_fill_bf16 ? p.logits_fill_bf16 + static_cast<int64_t>(r) * S : nullptr, sm);
 }
 
 // ===========================================================================
@@ -1825,6 +1840,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
     const float qs = n > 0 ? *qscale_sm : 0.f;
     float* lout = p.logits_out ? p.logits_out + static_cast<int64_t>(r) * S : nullptr;
+    uint16_t* lout16 = p.logits_bf16 ? p.logits_bf16 + static_cast<int64_t>(r) * S : nullptr;
     int e = 0;
     for (int ie = 0; ie < n && ok; ++ie) {
       const int a = ie % NA;
@@ -1860,6 +1876,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int col = c0 + lc;
         if (col < e) lg[col] = logit;
         if (lout && col < S) lout[col] = col < e ? logit : -INFINITY;
+        if (lout16 && col < S) lout16[col] = col < e ? to_bf16(logit) : kBf16NegInf;
       }
       if (warp == 2 && lane == 0 && ie == 0) SMQ_MARK(11);
       if (warp == 2 && lane == 0 && ie == n - 1) SMQ_MARK(12);
@@ -1993,6 +2010,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   int32_t* colo = p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr;
   if (rank == C - 1 && p.logits_out)  // columns past the last tile
     for (int c = T * kTileM + tid; c < S; c += kScoreThreads) p.logits_out[static_cast<int64_t>(r) * S + c] = -INFINITY;
+  if (rank == C - 1 && p.logits_bf16)
+    for (int c = T * kTileM + tid; c < S; c += kScoreThreads) p.logits_bf16[static_cast<int64_t>(r) * S + c] = kBf16NegInf;
   auto valid_cols = [&](int cr) {  // valid columns of CTA cr: [T cr / C * 256, ...) below e
     const int a = static_cast<int>(static_cast<int64_t>(T) * cr / C) * kTileM;
     const int b = static_cast<int>(static_cast<int64_t>(T) * (cr + 1) / C) * kTileM;
@@ -2035,7 +2054,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   sm.sidx = sidx;
   if (!warp_wait(bar_recv(0), 0, abort_flag, kWaitLimitNs)) set_status(p.status, kStatusTimeout);
   if (tid == 0) SMQ_MARK(14);
-  select_topk<kScoreThreads, kJ, true, true>(lg, S, end_sm, k, nullptr, p.nsb, sbkv, out, colo, nullptr, sm);
+  select_topk<kScoreThreads, kJ, true, true>(lg, S, end_sm, k, nullptr, p.nsb, sbkv, out, colo, nullptr, nullptr, sm);
   if (tid == 0) SMQ_MARK(16);
 }
 

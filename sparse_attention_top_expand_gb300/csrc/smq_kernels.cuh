@@ -114,6 +114,7 @@ struct ScoreParams {
   // row-cluster kernel: CTAs per row (the cluster size); logits_out, or null
   int32_t cluster;
   float* logits_out;
+  uint16_t* logits_bf16;  // when non-null: the logits rounded to bf16, -inf past end (the caller's logits_out_bf16)
   // outputs
   float* logits;     // [rows][num_cols]
   int32_t* status;   // workspace status word
@@ -128,6 +129,7 @@ struct TopkParams {
   int32_t num_cols;
   const float* logits;
   float* logits_fill;  // when non-null: write -inf to columns >= end (the caller's logits_out)
+  uint16_t* logits_fill_bf16;  // the same for the caller's bf16 logits
   const int32_t* sparse_indices;
   const int32_t* end;
   int32_t* topk_out;

@@ -361,6 +361,38 @@ def decode_batch(seed: int = 1, rows: int = 64) -> DecodeInputs:
     return _paged_decode(seed, rows, 64, 64, 128, 32, 2048, ctx, row_perm=False)
 
 
+def multi_token_decode(seed: int = 5, requests: int = 32, next_n: int = 2, num_heads: int = 64,
+                       page_size: int = 64, cbs: int = 128, ncb: int = 32, topk: int = 2048,
+                       ctx_range=(4096, 32768)) -> DecodeInputs:
+    """Decode with next_n query tokens per request (speculative decoding): rows
+    are request-major, row r is token r % next_n of request r // next_n, maps
+    to that request's block-table row through row_indices, and sees its causal
+    context: the request's length minus next_n, plus the token's index plus
+    one. Each row has its own ncb distinct candidate blocks below its end."""
+    d = HEAD_DIM
+    rng = _rng(seed)
+    geom = Geometry(num_heads, d, page_size, cbs, ncb, topk)
+    rows = requests * next_n
+    q, qs, w = _queries(rng, rows, num_heads, d)
+    ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=requests)
+    npages_req = [(int(c) + page_size - 1) // page_size for c in ctx]
+    num_pages = int(sum(npages_req))
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((requests, max(npages_req)), -1, dtype=np.int32)
+    off = 0
+    for j, n in enumerate(npages_req):
+        bt[j, :n] = perm[off:off + n]
+        off += n
+    row_indices = (np.arange(rows) // next_n).astype(np.int32)
+    row_ke = np.array([int(ctx[r // next_n]) - next_n + (r % next_n) + 1 for r in range(rows)], dtype=np.int32)
+    cand = np.empty((rows, ncb), dtype=np.int32)
+    for r in range(rows):
+        cand[r] = _distinct_blocks(rng, (int(row_ke[r]) + cbs - 1) // cbs, ncb)
+    touched = _touched_pages(bt, row_indices, row_ke, cand, cbs, page_size)
+    cache = _fill_cache(rng, num_pages, page_size, d, touched)
+    return DecodeInputs(geom, q, qs, w, cache, bt, row_indices, row_ke, cand)
+
+
 def long_context_decode(seed: int = 4, rows: int = 256) -> DecodeInputs:
     """256 rows, H=64, contexts log-uniform in [2048, 131072] with 10% of rows
     shorter than topk (uniform in [1, 2047]); cbs=128, 64 blocks per row
@@ -452,4 +484,5 @@ WORKLOADS = {
     "prefill_chunk": prefill_chunk,
     "shared_schedule": shared_schedule_layers,
     "long_context_decode": long_context_decode,
+    "multi_token_decode": multi_token_decode,
 }

@@ -33,7 +33,8 @@ def plan_for(geom, max_rows: int, device=None) -> Plan:
 class DecodeDevice:
     """Device copies of a DecodeInputs plus output buffers."""
 
-    def __init__(self, inp, plan: Plan, with_logits: bool = True, with_cols: bool = True):
+    def __init__(self, inp, plan: Plan, with_logits: bool = True, with_cols: bool = True,
+                 with_logits_bf16: bool = False):
         dev = plan.device
         R = inp.rows
         self.rows = R
@@ -51,6 +52,8 @@ class DecodeDevice:
         self.col_indices = torch.full((R, plan.topk), -7, dtype=torch.int32, device=dev) if with_cols else None
         self.logits = torch.full((R, plan.num_sparse_cols), float("nan"), dtype=torch.float32,
                                  device=dev) if with_logits else None
+        self.logits_bf16 = torch.full((R, plan.num_sparse_cols), 0x7FC1, dtype=torch.int16,
+                                      device=dev) if with_logits_bf16 else None
         self.workspace = plan.workspace(max(R, 1))
 
     def run(self, plan: Plan, expansion_ready: bool = False, stream=None) -> None:
@@ -58,7 +61,7 @@ class DecodeDevice:
                                       self.row_indices, self.row_ke, self.candidate_blocks, self.topk_out,
                                       self.sparse_indices, self.end, self.workspace,
                                       expansion_ready=expansion_ready, col_indices=self.col_indices,
-                                      logits_out=self.logits, stream=stream)
+                                      logits_out=self.logits, stream=stream, logits_out_bf16=self.logits_bf16)
 
     def expand(self, plan: Plan, stream=None) -> None:
         sparse_mqa_candidate_expand(plan, self.candidate_blocks, None, self.row_ke, self.sparse_indices, self.end,
@@ -68,7 +71,8 @@ class DecodeDevice:
 class PrefillDevice:
     """Device copies of a PrefillInputs (paged cache + gathered workspace) plus outputs."""
 
-    def __init__(self, inp, plan: Plan, with_logits: bool = True, with_cols: bool = True):
+    def __init__(self, inp, plan: Plan, with_logits: bool = True, with_cols: bool = True,
+                 with_logits_bf16: bool = False):
         dev = plan.device
         R = inp.rows
         self.rows = R
@@ -90,6 +94,8 @@ class PrefillDevice:
         self.col_indices = torch.full((R, plan.topk), -7, dtype=torch.int32, device=dev) if with_cols else None
         self.logits = torch.full((R, plan.num_sparse_cols), float("nan"), dtype=torch.float32,
                                  device=dev) if with_logits else None
+        self.logits_bf16 = torch.full((R, plan.num_sparse_cols), 0x7FC1, dtype=torch.int16,
+                                      device=dev) if with_logits_bf16 else None
         self.workspace = plan.workspace(max(R, 1))
 
     def gather(self, plan: Plan, stream=None) -> None:
@@ -101,7 +107,8 @@ class PrefillDevice:
                                              self.ks, self.ke, self.candidate_blocks, self.topk_out,
                                              self.sparse_indices, self.end, self.workspace,
                                              expansion_ready=expansion_ready, col_indices=self.col_indices,
-                                             logits_out=self.logits, stream=stream)
+                                             logits_out=self.logits, stream=stream,
+                                             logits_out_bf16=self.logits_bf16)
 
 
 def to_numpy(t: Optional[torch.Tensor]):

@@ -3,6 +3,7 @@
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 import oracle
 from oracle import check
@@ -32,6 +33,16 @@ def check_rows(inp, dev, plan, ref_rows, all_rows=True):
     nsb = plan.num_sparse_blocks
     rows = range(inp.rows) if all_rows else sorted(ref_rows)
     orc = oracle.default()
+    l16 = getattr(dev, "logits_bf16", None)
+    if l16 is not None:
+        # each bf16 logit is the call's own fp32 logit rounded to nearest even (torch's cast), -inf past end
+        assert logits is not None, "the bf16 logits are compared with the fp32 ones of the same call"
+        f32 = dev.logits
+        valid = torch.arange(f32.shape[1], device=f32.device)[None, :] < dev.end[:, None].long()
+        expect = f32.to(torch.bfloat16).view(torch.int16)
+        assert torch.equal(l16[valid], expect[valid]), "bf16 logits are the fp32 logits rounded to nearest even"
+        assert bool((l16[~valid] == -128).all()), "masked bf16 logits are -inf (0xFF80)"
+        l16 = l16.view(torch.bfloat16).to(torch.float64).cpu().numpy()
     for r in rows:
         if hasattr(inp, "row_ke"):
             L = int(inp.row_ke[r])
@@ -57,6 +68,8 @@ def check_rows(inp, dev, plan, ref_rows, all_rows=True):
             row = ref_rows[r]
             ref_logits = row.logits[row.positions] if row.valid is not None else row.logits
             check.check_logits(logits[r, :e], ref_logits, f"row {r} logits")
+            if l16 is not None:
+                check.check_logits_bf16(l16[r, :e], ref_logits, f"row {r} bf16 logits")
             check.check_topk(top[r], row, k, f"row {r} top-k")
 
 

@@ -26,7 +26,7 @@ def _ok(status):
 
 def test_tiny_decode_dense():
     inp = synth.tiny_decode(0)
-    plan, dev, status = run_decode(inp)
+    plan, dev, status = run_decode(inp, with_logits_bf16=True)
     _ok(status)
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
 
@@ -43,6 +43,8 @@ GEOMS = [
     (128, 32, 64, 12, 64, (500, 1500)),
     # more than 64 candidate blocks: expansion and top-k in their own kernels (16384 columns)
     (64, 64, 128, 128, 2048, (14000, 20000)),
+    # 8448 columns: too wide for a row cluster; the persistent kernel expands and selects itself
+    (64, 64, 256, 33, 300, (5000, 9000)),
 ]
 
 
@@ -54,7 +56,7 @@ def test_decode_geometries_dense(geom):
     ctx = rng.integers(lo, hi + 1, size=rows)
     inp = synth._paged_decode(seed=h + page, rows=rows, h=h, page_size=page, cbs=cbs, ncb=ncb, topk=topk,
                               ctx=ctx, row_perm=True)
-    plan, dev, status = run_decode(inp)
+    plan, dev, status = run_decode(inp, with_logits_bf16=True)
     _ok(status)
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
 
@@ -107,6 +109,20 @@ def test_prefill_expansion_of_repeated_negative_and_out_of_range_ids():
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
 
 
+@pytest.mark.parametrize("next_n,requests", [(2, 12), (4, 9), (3, 60)])
+def test_multi_token_decode_rows(next_n, requests):
+    """next_n query tokens per request (speculative decoding): the rows of a
+    request share its block-table row through row_indices, and each sees its
+    own causal context. 180 rows take the persistent kernel and the top-k
+    kernel; fewer take one cluster per row."""
+    inp = synth.multi_token_decode(seed=60 + next_n, requests=requests, next_n=next_n, ctx_range=(300, 6000),
+                                   ncb=12, topk=500)
+    assert len(set(inp.row_indices.tolist())) == requests and inp.block_table.shape[0] == requests
+    plan, dev, status = run_decode(inp, with_logits_bf16=True)
+    _ok(status)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense"))
+
+
 def test_decode_batch_full_size():
     """64 rows, H=64, contexts 4096..32768, 32 blocks of 128, topk 2048."""
     inp = synth.decode_batch()
@@ -131,7 +147,7 @@ def test_long_context_full_size():
 def test_prefill_small_dense():
     inp = synth.prefill_chunk(seed=12, seq_lens=(1500, 2300, 700), queries_per_seq=40, num_heads=64,
                               page_size=64, cbs=128, ncb=6, topk=300)
-    plan, dev, status = run_prefill(inp)
+    plan, dev, status = run_prefill(inp, with_logits_bf16=True)
     _ok(status)
     kv, ks = oracle.gather_reference(inp)
     assert np.array_equal(tensors.to_numpy(dev.k_values), kv)
