@@ -20,6 +20,9 @@ Parity status of each function (the pins live in ``tests/test_oracle_pins.py``):
   - gather: numpy slicing of the page bytes.
   - dense-then-masked == candidate-only: an invariant checked on every small
     workload.
+  - candidate source (block scores, published blocks): hand-worked maxima
+    through the one-hot closed form; the monotone and all-equal keys;
+    a short context; brute-force ranking by numpy.
   - producers (K-cache writer, query quantiser): E2M1 / E4M3 / bf16 encoders
     against the value tables' midpoints and torch's float8_e4m3fn / bfloat16
     casts; hand-worked scale exponents; nearest-grid-point brute force; the
@@ -109,6 +112,8 @@ class Oracle:
                                                  ctypes.c_int64]
         lib.smq_oracle_quantize_q.restype = ctypes.c_int
         lib.smq_oracle_quantize_q.argtypes = [ctypes.c_int, ctypes.c_int, _u16p, _f32p, _u8p, _f32p, _u16p]
+        lib.smq_oracle_source_blocks.restype = ctypes.c_int
+        lib.smq_oracle_source_blocks.argtypes = [ctypes.c_int64, _f64p, ctypes.c_int, ctypes.c_int, _f64p, _i32p]
         lib.smq_oracle_gather.restype = ctypes.c_int
         lib.smq_oracle_gather.argtypes = [
             ctypes.c_int, ctypes.c_int, _u8p, ctypes.c_int64, _i32p, ctypes.c_int64,
@@ -174,6 +179,18 @@ class Oracle:
             if rc != 0:
                 raise ValueError(f"oracle: non-finite query or weight in row {r}")
         return q8, sc, wb
+
+    def source_blocks(self, logits: np.ndarray, cbs: int, ncb: int):
+        """A row's dense logits [L] -> (its ncb published blocks, each block's maximum logit)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float64)
+        L = len(logits)
+        nb = (L + cbs - 1) // cbs
+        scores = np.empty(max(nb, 1), dtype=np.float64)
+        cand = np.empty(ncb, dtype=np.int32)
+        if self.lib.smq_oracle_source_blocks(L, _ptr(logits, _f64p), cbs, ncb, _ptr(scores, _f64p),
+                                             _ptr(cand, _i32p)) != 0:
+            raise MemoryError("oracle source blocks")
+        return cand, scores[:nb]
 
     # -- per-row primitives -------------------------------------------------
     def logits_paged(self, inp, r: int, p0: int, p1: int) -> np.ndarray:
@@ -343,6 +360,26 @@ def reference_rows(inp, rows: Optional[Iterable[int]] = None, mode: str = "spars
     threads = threads or os.cpu_count() or 1
     with ThreadPoolExecutor(max_workers=threads) as ex:
         res = list(ex.map(lambda r: _row_reference(orc, inp, r, mode, contig), rows))
+    return dict(zip(rows, res))
+
+
+def source_rows(inp, rows: Optional[Iterable[int]] = None, threads: Optional[int] = None,
+                orc: Optional[Oracle] = None):
+    """The candidate source of decode rows: dense logits over each row's whole
+    context, then its published blocks. Returns {row: (cand [ncb], block
+    scores, dense logits)}."""
+    orc = orc or default()
+    g = inp.geom
+    rows = list(range(inp.rows)) if rows is None else list(rows)
+
+    def one(r):
+        L = max(int(inp.row_ke[r]), 0)
+        logits = orc.logits_paged(inp, r, 0, L)
+        cand, scores = orc.source_blocks(logits, g.candidate_block_size, g.candidate_topk_blocks)
+        return cand, scores, logits
+
+    with ThreadPoolExecutor(max_workers=threads or os.cpu_count() or 1) as ex:
+        res = list(ex.map(one, rows))
     return dict(zip(rows, res))
 
 

@@ -459,3 +459,47 @@ int smq_oracle_quantize_q(int H, int D, const uint16_t *q, const float *w, uint8
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Candidate source
+ * ------------------------------------------------------------------------- */
+
+/* The candidate-source indexer of two-level selection: a dense indexer over
+ * the row's whole context that publishes its top candidate blocks
+ * ("sparse_mqa_indexer" docs, module docstring; "rocm_paged_mxfp4_indexer"
+ * docs, RocmSparseAttnIndexer: the source layer publishes its candidate
+ * pool, candidate_write). The pages do not define a block's score. The
+ * reading taken here: the score of block b (positions [b*cbs, (b+1)*cbs)
+ * below L) is the largest dense logit among its positions; the ncb blocks of
+ * highest score are published, ties to the lower block id, in that order,
+ * then -1 when the context has fewer blocks. */
+typedef struct {
+  double v;
+  int64_t b;
+} scored_block;
+
+static int by_score_desc_id_asc(const void *a, const void *b) {
+  const scored_block *x = (const scored_block *)a;
+  const scored_block *y = (const scored_block *)b;
+  if (x->v != y->v) return x->v > y->v ? -1 : 1;
+  return (x->b > y->b) - (x->b < y->b);
+}
+
+int smq_oracle_source_blocks(int64_t L, const double *logits, int cbs, int ncb, double *block_scores,
+                             int32_t *cand) {
+  int64_t nb = L > 0 ? (L + cbs - 1) / cbs : 0;
+  scored_block *s = (scored_block *)malloc(sizeof(scored_block) * (size_t)(nb ? nb : 1));
+  if (!s) return -1;
+  for (int64_t b = 0; b < nb; ++b) {
+    double m = -INFINITY;
+    for (int64_t p = b * cbs; p < (b + 1) * cbs && p < L; ++p)
+      if (logits[p] > m) m = logits[p];
+    s[b].v = m;
+    s[b].b = b;
+    if (block_scores) block_scores[b] = m;
+  }
+  qsort(s, (size_t)nb, sizeof(scored_block), by_score_desc_id_asc);
+  for (int i = 0; i < ncb; ++i) cand[i] = i < nb ? (int32_t)s[i].b : -1;
+  free(s);
+  return 0;
+}

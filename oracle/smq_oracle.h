@@ -107,6 +107,13 @@ int smq_oracle_write_k_cache(int D, int page_size, const uint16_t *k, const int6
 int smq_oracle_quantize_q(int H, int D, const uint16_t *q, const float *w, uint8_t *q8, float *scale,
                           uint16_t *w_bf16);
 
+/* Candidate source: the ncb blocks (of cbs positions) of a row's dense
+ * logits [L] with the largest maximum logit, ties to the lower block id, in
+ * that order, then -1. block_scores [ceil(L / cbs)] (may be NULL) receives
+ * each block's maximum. */
+int smq_oracle_source_blocks(int64_t L, const double *logits, int cbs, int ncb, double *block_scores,
+                             int32_t *cand);
+
 #ifdef __cplusplus
 }
 #endif

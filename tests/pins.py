@@ -34,6 +34,13 @@ What pins what:
                            one-hot query reads the written keys back
   q_quantiser              torch: scale = amax / 448 in float32, codes of
                            x / scale cast to float8_e4m3fn, bf16 weights
+  source_hand              candidate source, hand-worked: block maxima set
+                           through the one-hot closed form, a tie, a partial
+                           last block, a block of zeros, -1 padding
+  source_monotone_ties     increasing keys -> the last blocks first; equal
+                           keys -> the first blocks
+  source_numpy             random logits: numpy block maxima (padded with
+                           -inf) and a lexsort on (-max, block id)
 """
 
 from __future__ import annotations
@@ -495,8 +502,57 @@ def pin_q_quantiser(orc):
     assert np.array_equal(wb, _bf16_bits(w)), "bf16 weights"
 
 
+# -------------------------------------------------------------- candidate source
+
+
+def pin_source_hand(orc):
+    """One head, one-hot query at d = 5: L[p] = max(0, K[p, 5]). cbs = 16,
+    L = 75 (five blocks, the last of 11 positions). Block maxima by hand:
+    1.0, 3.0, 0, 3.0, 6.0 -> blocks 4, 1, 3 (tie with 1, higher id), 0, 2, then -1."""
+    inp = _blank_decode(8, 16, 6, 75, 7, 16, 4)
+    inp.q[0, 0, 5] = E4M3_ONE
+    inp.weights[0, 1:] = 0
+    # (position, E2M1 code): 1.0 = code 2, 3.0 = code 5, 6.0 = code 7, 0.5 = code 1, -6 = code 15
+    for p, code in [(3, 2), (7, 1), (20, 5), (31, 2), (40, 15), (50, 5), (49, 1), (74, 7), (66, 5)]:
+        _set_key(inp, p, 5, code, 127)
+    cand, scores, logits = orc_source_row(orc, inp)
+    assert scores.tolist() == [1.0, 3.0, 0.0, 3.0, 6.0], f"block maxima {scores.tolist()}"
+    assert cand.tolist() == [4, 1, 3, 0, 2, -1, -1], f"published blocks {cand.tolist()}"
+
+
+def orc_source_row(orc, inp):
+    return oracle_pkg.source_rows(inp, rows=[0], orc=orc)[0]
+
+
+def pin_source_monotone_ties(orc):
+    inp = _monotone_input(90, [-1] * 4, 8)  # cbs 16: blocks 0..5, the last of 10 positions
+    inp.geom = synth.Geometry(1, 128, 16, 16, 4, 8)
+    cand, scores, logits = orc_source_row(orc, inp)
+    assert cand.tolist() == [5, 4, 3, 2], f"increasing keys: {cand.tolist()}"
+    flat = _blank_decode(8, 16, 6, 64, 6, 16, 4)  # every key zero: every logit 0, every block ties
+    cand, scores, logits = orc_source_row(orc, flat)
+    assert cand.tolist() == [0, 1, 2, 3, -1, -1], f"equal keys: {cand.tolist()}"
+
+
+def pin_source_numpy(orc):
+    rng = np.random.Generator(np.random.PCG64(37))
+    for L, cbs, ncb in [(1000, 64, 8), (97, 16, 10), (5, 16, 3), (4096, 128, 32), (130, 128, 4)]:
+        logits = np.round(rng.standard_normal(L), 1)  # rounding makes block-maximum ties
+        cand, scores = orc.source_blocks(logits, cbs, ncb)
+        nb = -(-L // cbs)
+        padded = np.full(nb * cbs, -np.inf)
+        padded[:L] = logits
+        mx = padded.reshape(nb, cbs).max(axis=1)
+        assert np.array_equal(scores, mx), f"block maxima L={L}"
+        order = np.lexsort((np.arange(nb), -mx))[:ncb]
+        want = np.full(ncb, -1)
+        want[:len(order)] = order
+        assert np.array_equal(cand, want), f"published blocks L={L}: {cand.tolist()} != {want.tolist()}"
+
+
 ALL_PINS = [
     pin_e4m3, pin_bf16, pin_e2m1, pin_ue8m0, pin_one_hot, pin_relu_sign, pin_exact_rational,
     pin_numpy_einsum, pin_monotone_topk, pin_ties, pin_padding, pin_expansion_golden, pin_gather,
     pin_dense_equals_sparse, pin_encoders, pin_k_scale_cases, pin_k_nearest, pin_k_cache_layout, pin_q_quantiser,
+    pin_source_hand, pin_source_monotone_ties, pin_source_numpy,
 ]

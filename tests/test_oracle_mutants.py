@@ -60,6 +60,10 @@ MUTANTS = {
     "q scale 447": ("float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
     "q zero-row scale": ("float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 448.0f : 0.5f;"),
     "bf16 ties down": ("if (dhi < dlo || (dhi == dlo && (hi & 1) == 0)) return hi;", "if (dhi < dlo) return hi;"),
+    "source ties to the higher id": ("return (x->b > y->b) - (x->b < y->b);", "return (x->b < y->b) - (x->b > y->b);"),
+    "source block sum": ("if (logits[p] > m) m = logits[p];", "m = (m == -INFINITY ? 0.0 : m) + logits[p];"),
+    "source partial block dropped": ("int64_t nb = L > 0 ? (L + cbs - 1) / cbs : 0;", "int64_t nb = L > 0 ? L / cbs : 0;"),
+    "source no -1 pad": ("cand[i] = i < nb ? (int32_t)s[i].b : -1;", "cand[i] = i < nb ? (int32_t)s[i].b : 0;"),
     "gather scale offset": ("base + (int64_t)page_size * (D / 2) + tok * (D / 32),\n           (size_t)(D / 32));",
                             "base + (int64_t)page_size * (D / 2),\n           (size_t)(D / 32));"),
 }
