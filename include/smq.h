@@ -293,6 +293,49 @@ SMQ_API int sparse_mqa_gather_k(const smq_plan *plan, const uint8_t *k_cache, in
                                 uint8_t *k_values, uint8_t *k_scales, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* The candidate source of two-level selection, on paged decode rows: a
+ * dense indexer over each row's whole context [0, row_ke) that publishes the
+ * row's best candidate blocks for the consumer calls above. (Source:
+ * sparse_mqa_indexer docs, module docstring: the candidate-source indexer
+ * publishes the top candidate blocks and later indexers pick their top-k
+ * inside them; rocm_paged_mxfp4_indexer docs, RocmSparseAttnIndexer: the
+ * source layer publishes its candidate pool, candidate_write.) The pages do
+ * not define a block's score. This library's: block b (positions
+ * [b * cbs, (b + 1) * cbs) below row_ke) scores its largest logit, the
+ * logit being the one the consumer calls compute. Each row publishes its
+ * candidate_topk_blocks best blocks, best first, ties to the lower block id,
+ * then -1 when the context has fewer blocks. */
+typedef struct smq_source_args {
+  uint32_t struct_size;
+  int32_t rows;                   /* R >= 0 */
+  const uint8_t *q;               /* device [R][H][D] E4M3 */
+  const float *q_scale;           /* device [R] */
+  const uint16_t *weights;        /* device [R][H] bf16 */
+  const uint8_t *k_cache;         /* device [num_pages][page_bytes], 16-byte aligned */
+  int64_t num_pages;
+  const int32_t *block_table;     /* device [bt_rows][bt_stride] */
+  int32_t bt_rows;
+  int32_t bt_stride;
+  const int32_t *row_indices;     /* device [R] row -> block-table row, or NULL = identity */
+  const int32_t *row_ke;          /* device [R] context length; a longer context than max_context
+                                     raises SMQ_ERR_BOUNDS and is cut there */
+  int32_t max_context;            /* the longest context of the call, 1 .. 1048576 */
+  int32_t *candidate_blocks;      /* device [R][candidate_topk_blocks] out */
+  float *block_scores;            /* device [R][ceil(max_context / cbs)] out (-inf past a row's
+                                     blocks), or NULL */
+  void *workspace;                /* device, >= smq_source_workspace_size(plan, R, max_context) */
+  size_t workspace_bytes;
+} smq_source_args;
+
+/* Workspace bytes of a candidate-source call: the status word, the dense
+ * layout of the rows and their fp32 logits [rows][max_context rounded up
+ * to whole blocks]. Zero it with smq_workspace_init before the first call.
+ * ceil(max_context / cbs) may not exceed 8192. */
+SMQ_API int smq_source_workspace_size(const smq_plan *plan, int32_t rows, int32_t max_context, size_t *bytes);
+
+SMQ_API int sparse_mqa_candidate_source_decode(const smq_plan *plan, const smq_source_args *args,
+                                               void *stream);
+
 /* Producers of the indexer's inputs. (Source: sparse_mqa_indexer docs,
  * SparseMQAIndexer and weights_dtype: the model writes the MXFP4 indexer K
  * cache, and a fused query kernel writes the FP8 query, its scale and the

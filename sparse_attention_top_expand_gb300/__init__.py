@@ -64,11 +64,20 @@ class SMQPrefillArgs(ctypes.Structure):
                 ("profile_events", _vp * 4), ("logits_out_bf16", _vp)]
 
 
+class SMQSourceArgs(ctypes.Structure):
+    _fields_ = [("struct_size", _c_u32), ("rows", _c_i32), ("q", _vp), ("q_scale", _vp), ("weights", _vp),
+                ("k_cache", _vp), ("num_pages", _c_i64), ("block_table", _vp), ("bt_rows", _c_i32),
+                ("bt_stride", _c_i32), ("row_indices", _vp), ("row_ke", _vp), ("max_context", _c_i32),
+                ("candidate_blocks", _vp), ("block_scores", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 EXPORTED = [
     "smq_plan_create", "smq_plan_destroy", "smq_plan_get_info", "smq_workspace_size", "smq_workspace_init",
     "smq_get_status", "smq_error_string", "sparse_mqa_candidate_expand", "sparse_mqa_logits_topk_decode",
     "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k", "sparse_mqa_logits_topk_decode_noalloc",
-    "sparse_mqa_write_k_cache", "sparse_mqa_quantize_q",
+    "sparse_mqa_write_k_cache", "sparse_mqa_quantize_q", "smq_source_workspace_size",
+    "sparse_mqa_candidate_source_decode",
 ]
 
 _lib = None
@@ -99,6 +108,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.c_size_t, _vp]
     lib.sparse_mqa_write_k_cache.argtypes = [_vp, _vp, _vp, _c_i64, _vp, _c_i64, _vp, ctypes.c_size_t, _vp]
     lib.sparse_mqa_quantize_q.argtypes = [_vp, _vp, _vp, _c_i32, _vp, _vp, _vp, _vp]
+    lib.smq_source_workspace_size.argtypes = [_vp, _c_i32, _c_i32, P(ctypes.c_size_t)]
+    lib.sparse_mqa_candidate_source_decode.argtypes = [_vp, P(SMQSourceArgs), _vp]
     for name in EXPORTED:
         if name != "smq_error_string":
             getattr(lib, name).restype = ctypes.c_int
@@ -378,3 +389,38 @@ def sparse_mqa_quantize_q(plan: Plan, q, weights, q_fp8, q_scale, weights_bf16, 
         plan.handle, _ptr(q, _BF16, "q", dev), _ptr(weights, _F32, "weights", dev), int(q.shape[0]),
         _ptr(q_fp8, _U8, "q_fp8", dev), _ptr(q_scale, _F32, "q_scale", dev),
         _ptr(weights_bf16, _BF16, "weights_bf16", dev), _stream(stream)), "sparse_mqa_quantize_q")
+
+
+def smq_source_workspace_size(plan: Plan, rows: int, max_context: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().smq_source_workspace_size(plan.handle, rows, max_context, ctypes.byref(n)),
+           "smq_source_workspace_size")
+    return n.value
+
+
+def sparse_mqa_candidate_source_decode(plan: Plan, q, q_scale, weights, k_cache, block_table, row_indices, row_ke,
+                                       max_context: int, candidate_blocks, workspace, block_scores=None,
+                                       stream=None) -> None:
+    """The candidate source: dense scores over each row's context, then the row's
+    candidate_topk_blocks best blocks of candidate_block_size positions."""
+    dev = plan.device
+    a = SMQSourceArgs()
+    a.struct_size = ctypes.sizeof(SMQSourceArgs)
+    a.rows = int(q.shape[0])
+    a.q = _ptr(q, _U8, "q", dev)
+    a.q_scale = _ptr(q_scale, _F32, "q_scale", dev)
+    a.weights = _ptr(weights, _BF16, "weights", dev)
+    a.k_cache = _ptr(k_cache, _U8, "k_cache", dev)
+    a.num_pages = int(k_cache.shape[0])
+    a.block_table = _ptr(block_table, _I32, "block_table", dev)
+    a.bt_rows = int(block_table.shape[0])
+    a.bt_stride = int(block_table.shape[1])
+    a.row_indices = _ptr(row_indices, _I32, "row_indices", dev)
+    a.row_ke = _ptr(row_ke, _I32, "row_ke", dev)
+    a.max_context = int(max_context)
+    a.candidate_blocks = _ptr(candidate_blocks, _I32, "candidate_blocks", dev)
+    a.block_scores = _ptr(block_scores, _F32, "block_scores", dev)
+    a.workspace = _ptr(workspace, _U8, "workspace", dev)
+    a.workspace_bytes = workspace.numel()
+    _check(load_library().sparse_mqa_candidate_source_decode(plan.handle, ctypes.byref(a), _stream(stream)),
+           "sparse_mqa_candidate_source_decode")

@@ -605,6 +605,114 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan* plan, const sm
   return sparse_mqa_logits_topk_decode(plan, &a, stream);
 }
 
+namespace {
+
+// The candidate source's dense layout: whole blocks covering max_context.
+struct SourceLayout {
+  int32_t num_cols, nsb, max_blocks;
+  size_t si_off, end_off, logits_off, total;
+};
+
+bool source_layout(const smq_plan* p, int64_t rows, int64_t max_context, SourceLayout* out) {
+  if (max_context <= 0 || max_context > (int64_t(1) << 20) || rows < 0) return false;
+  const int64_t cbs = p->desc.candidate_block_size;
+  const int64_t blocks = (max_context + cbs - 1) / cbs;
+  if (blocks > smq::kSourceMaxBlocks) return false;
+  out->max_blocks = static_cast<int32_t>(blocks);
+  out->num_cols = static_cast<int32_t>(blocks * cbs);
+  out->nsb = out->num_cols / p->sbkv;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  out->si_off = kStatusBytes + counter_bytes(p);
+  out->end_off = out->si_off + up(static_cast<size_t>(rows) * out->nsb * 4);
+  out->logits_off = out->end_off + up(static_cast<size_t>(rows) * 4);
+  out->total = out->logits_off + static_cast<size_t>(rows) * out->num_cols * 4;
+  return true;
+}
+
+}  // namespace
+
+SMQ_API int smq_source_workspace_size(const smq_plan* plan, int32_t rows, int32_t max_context, size_t* bytes) {
+  if (!plan || !bytes || rows < 0 || rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  SourceLayout l;
+  if (!source_layout(plan, rows, max_context, &l)) return SMQ_ERR_UNSUPPORTED;
+  *bytes = l.total;
+  return SMQ_OK;
+}
+
+SMQ_API int sparse_mqa_candidate_source_decode(const smq_plan* plan, const smq_source_args* args, void* stream) {
+  if (!plan || !args || args->struct_size < sizeof(smq_source_args)) return SMQ_ERR_INVALID_ARG;
+  const smq_source_args& a = *args;
+  if (a.rows < 0 || a.rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
+  if (a.rows == 0) return SMQ_OK;
+  SourceLayout l;
+  if (!source_layout(plan, a.rows, a.max_context, &l)) return SMQ_ERR_UNSUPPORTED;
+  if (!a.q || !a.q_scale || !a.weights || !a.k_cache || !a.block_table || !a.row_ke || !a.candidate_blocks ||
+      !a.workspace || a.num_pages <= 0 || a.bt_rows <= 0 || a.bt_stride <= 0)
+    return SMQ_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.weights, 16) || !aligned(a.k_cache, 16) || !aligned(a.workspace, 16) ||
+      !aligned(a.q_scale, 4) || !aligned(a.block_table, 4) || !aligned(a.candidate_blocks, 4) ||
+      (a.block_scores && !aligned(a.block_scores, 4)))
+    return SMQ_ERR_INVALID_ARG;
+  if (a.workspace_bytes < l.total) return SMQ_ERR_WORKSPACE_TOO_SMALL;
+  int rc = check_device(const_cast<smq_plan*>(plan));
+  if (rc != SMQ_OK) return rc;
+  if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  smq::SourceParams sp;
+  std::memset(&sp, 0, sizeof sp);
+  sp.rows = a.rows;
+  sp.sbkv = plan->sbkv;
+  sp.nsb = l.nsb;
+  sp.num_cols = l.num_cols;
+  sp.cbs = plan->desc.candidate_block_size;
+  sp.ncb = plan->desc.candidate_topk_blocks;
+  sp.max_blocks = l.max_blocks;
+  sp.row_ke = a.row_ke;
+  sp.sparse_indices = reinterpret_cast<int32_t*>(ws + l.si_off);
+  sp.end = reinterpret_cast<int32_t*>(ws + l.end_off);
+  sp.logits = reinterpret_cast<float*>(ws + l.logits_off);
+  sp.candidate_blocks = a.candidate_blocks;
+  sp.block_scores = a.block_scores;
+  sp.status = static_cast<int32_t*>(a.workspace);
+  if (smq::launch_source_layout(sp, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  // the dense rows through the score kernel, its sub-blocks read from the layout
+  CUtensorMap tm_q, tm_k;
+  std::memset(&tm_k, 0, sizeof tm_k);
+  rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
+  if (rc != SMQ_OK) return rc;
+  smq::ScoreParams p;
+  std::memset(&p, 0, sizeof p);
+  p.rows = a.rows;
+  p.heads = plan->desc.num_heads;
+  p.n_mma = plan->n_mma;
+  p.sbkv = plan->sbkv;
+  p.subs_per_tile = kTileM / plan->sbkv;
+  p.nsb = l.nsb;
+  p.num_cols = l.num_cols;
+  p.tmem_cols = smq::score_tmem_columns(plan->n_mma);
+  p.q_scale = a.q_scale;
+  p.weights = a.weights;
+  p.sparse_indices = sp.sparse_indices;
+  p.end = sp.end;
+  p.k_cache = a.k_cache;
+  p.num_pages = a.num_pages;
+  p.page_bytes = plan->page_bytes;
+  p.page_size = plan->desc.page_size;
+  p.bt_rows = a.bt_rows;
+  p.bt_stride = a.bt_stride;
+  p.block_table = a.block_table;
+  p.row_indices = a.row_indices;
+  p.logits = const_cast<float*>(sp.logits);
+  p.status = sp.status;
+  p.row_done = reinterpret_cast<int32_t*>(ws + kStatusBytes);
+  const int64_t tiles = static_cast<int64_t>(a.rows) * ((l.num_cols + kTileM - 1) / kTileM);
+  const int grid = static_cast<int>(tiles < plan->num_sms ? tiles : plan->num_sms);
+  const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
+  if (smq::launch_score(p, true, false, tm_q, tm_k, grid, smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
+  return smq::launch_source_select(sp, s) == cudaSuccess ? SMQ_OK : SMQ_ERR_CUDA;
+}
+
 SMQ_API int sparse_mqa_write_k_cache(const smq_plan* plan, const uint16_t* k, const int64_t* slot_mapping,
                                      int64_t ntok, uint8_t* k_cache, int64_t num_pages, void* workspace,
                                      size_t workspace_bytes, void* stream) {

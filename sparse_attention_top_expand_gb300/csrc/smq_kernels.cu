@@ -2059,6 +2059,77 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 }
 
 // ===========================================================================
+// Candidate source: dense layout, then block maxima and the best blocks.
+// ===========================================================================
+// One warp per row: sub-block j of the row's context is sparse sub-block j
+// (every position a column, in order); end = the context length.
+__global__ void __launch_bounds__(256) source_layout_kernel(const __grid_constant__ SourceParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= p.rows) return;
+  int L = p.row_ke[r];
+  if (L > p.num_cols) {
+    if (lane == 0) set_status(p.status, kStatusBounds);  // a context longer than the call's bound
+    L = p.num_cols;
+  }
+  L = L < 0 ? 0 : L;
+  int32_t* si = p.sparse_indices + static_cast<int64_t>(r) * p.nsb;
+  for (int j = lane; j < p.nsb; j += 32) si[j] = j * p.sbkv < L ? j : -1;
+  if (lane == 0) p.end[r] = L;
+}
+
+// One CTA per row: block b's score is the largest logit of its positions
+// below the row's end; the ncb best blocks (ties to the lower id) come out in
+// that order, then -1. Keys (score order, then the complement of the block
+// id) are sorted in shared memory, descending, by a bitonic network.
+__global__ void __launch_bounds__(512) source_select_kernel(const __grid_constant__ SourceParams p) {
+  extern __shared__ uint64_t src_keys[];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int L = p.end[r];
+  L = L < 0 ? 0 : (L > p.num_cols ? p.num_cols : L);
+  const int nb = (L + p.cbs - 1) / p.cbs;
+  int n2 = 1;
+  while (n2 < nb) n2 <<= 1;
+  const float* lg = p.logits + static_cast<int64_t>(r) * p.num_cols;
+  for (int b = warp; b < nb; b += 16) {  // a warp per block
+    float m = -INFINITY;
+    const int lo = b * p.cbs, hi = min(L, lo + p.cbs);
+    for (int c = lo + lane; c < hi; c += 32) m = fmaxf(m, __ldcg(lg + c));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+    if (lane == 0) {
+      src_keys[b] = (static_cast<uint64_t>(ordered_key(m)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(b));
+      if (p.block_scores) p.block_scores[static_cast<int64_t>(r) * p.max_blocks + b] = m;
+    }
+  }
+  for (int b = nb + tid; b < n2; b += 512) src_keys[b] = 0;  // below every block
+  if (p.block_scores)
+    for (int b = nb + tid; b < p.max_blocks; b += 512) p.block_scores[static_cast<int64_t>(r) * p.max_blocks + b] = -INFINITY;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < n2; i += 512) {
+        const int x = i ^ j;
+        if (x > i) {
+          const uint64_t a = src_keys[i], b = src_keys[x];
+          const bool desc = (i & k) == 0;  // descending runs where bit k of i is clear
+          if ((a < b) == desc) {
+            src_keys[i] = b;
+            src_keys[x] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  int32_t* out = p.candidate_blocks + static_cast<int64_t>(r) * p.ncb;
+  for (int i = tid; i < p.ncb; i += 512)
+    out[i] = i < nb ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(src_keys[i] & 0xFFFFFFFFu)) : -1;
+}
+
+// ===========================================================================
 // Launchers
 // ===========================================================================
 cudaError_t prepare_kernels(int n_mma) {
@@ -2078,7 +2149,9 @@ cudaError_t prepare_kernels(int n_mma) {
                        reinterpret_cast<const void*>(&topk_kernel<512, 16>),
                        reinterpret_cast<const void*>(&topk_kernel<512, 32>),
                        reinterpret_cast<const void*>(&expand_kernel),
-                       reinterpret_cast<const void*>(&gather_kernel)};
+                       reinterpret_cast<const void*>(&gather_kernel),
+                       reinterpret_cast<const void*>(&source_layout_kernel),
+                       reinterpret_cast<const void*>(&source_select_kernel)};
   for (const void* f : all) {
     err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
@@ -2108,6 +2181,9 @@ cudaError_t prepare_kernels(int n_mma) {
   }
   if (err != cudaSuccess) return err;
 
+  err = cudaFuncSetAttribute(source_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSourceMaxBlocks * 8);
+  if (err != cudaSuccess) return err;
   return cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kExpandWarps * 2 * 512 * 4);
 }
@@ -2201,6 +2277,16 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   if (p.num_cols <= 16 * 512) return launch_pdl(topk_kernel<512, 16>, p.rows, 512, smem, stream, p);
   static_assert(32 * 512 >= kMaxSparseCols, "the widest top-k kernel covers every row");
   return launch_pdl(topk_kernel<512, 32>, p.rows, 512, smem, stream, p);
+}
+
+cudaError_t launch_source_layout(const SourceParams& p, cudaStream_t stream) {
+  return launch_pdl(source_layout_kernel, static_cast<unsigned>((p.rows + 7) / 8), 256, 0, stream, p);
+}
+
+cudaError_t launch_source_select(const SourceParams& p, cudaStream_t stream) {
+  int n2 = 1;
+  while (n2 < p.max_blocks) n2 <<= 1;
+  return launch_pdl(source_select_kernel, static_cast<unsigned>(p.rows), 512, static_cast<size_t>(n2) * 8, stream, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {

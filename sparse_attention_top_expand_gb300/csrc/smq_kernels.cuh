@@ -188,6 +188,29 @@ struct QQuantParams {
   uint16_t* weights_out;
 };
 
+// The candidate source: every position of a row as a sparse column, then
+// each block's maximum logit and the row's best blocks.
+struct SourceParams {
+  int32_t rows;
+  int32_t sbkv;
+  int32_t nsb;          // sub-blocks per row of the dense layout
+  int32_t num_cols;     // nsb * sbkv
+  int32_t cbs;
+  int32_t ncb;          // blocks published per row
+  int32_t max_blocks;   // num_cols / cbs
+  const int32_t* row_ke;
+  int32_t* sparse_indices;  // [rows][nsb] the dense layout: sub-block j, or -1 past the row
+  int32_t* end;             // [rows]
+  const float* logits;      // [rows][num_cols]
+  int32_t* candidate_blocks;  // [rows][ncb]
+  float* block_scores;        // [rows][max_blocks], may be null
+  int32_t* status;
+};
+
+constexpr int kSourceMaxBlocks = 8192;  // blocks per row the selection sorts in shared memory
+cudaError_t launch_source_layout(const SourceParams& p, cudaStream_t stream);
+cudaError_t launch_source_select(const SourceParams& p, cudaStream_t stream);
+
 cudaError_t launch_write_k_cache(const KWriteParams& p, cudaStream_t stream);
 cudaError_t launch_quantize_q(const QQuantParams& p, cudaStream_t stream);
 

@@ -51,6 +51,7 @@ def test_struct_layouts_match_binding(tmp_path):
     fields = {
         "smq_plan_desc": smq.SMQPlanDesc, "smq_plan_info": smq.SMQPlanInfo,
         "smq_decode_args": smq.SMQDecodeArgs, "smq_prefill_args": smq.SMQPrefillArgs,
+        "smq_source_args": smq.SMQSourceArgs,
     }
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "smq.h"', 'int main(void) {']
     for cname, cls in fields.items():
