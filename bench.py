@@ -226,6 +226,8 @@ def make_inputs(workload: str, rank: int):
         return synth.prefill_as_decode(synth.prefill_chunk(seed=rank_seed(2, rank)))
     if workload == "shared_schedule":
         return synth.shared_schedule_layers(seed=rank_seed(3, rank))
+    if workload == "multi_token_decode":  # 32 requests x 2 query tokens (speculative decoding)
+        return synth.multi_token_decode(seed=rank_seed(5, rank), requests=32, next_n=2)
     raise SystemExit(f"unknown workload {workload}")
 
 
@@ -474,7 +476,7 @@ def measure(workload, args, rank, world, dist, device, steps, warmup, headline):
                 "time": "mean consumer-layer launch (events inside the timed graph)",
                 "kernel": "row_cluster_kernel per consumer layer"}
 
-    decode_like = workload in ("decode_batch", "long_context_decode", "tiny_decode")
+    decode_like = workload in ("decode_batch", "long_context_decode", "tiny_decode", "multi_token_decode")
     e2e = run_e2e(args, plan, base, cols, dist, device) if (decode_like and args.e2e_steps > 0) else None
     cpu = (run_cpu_baseline(base, workload, args.cpu_seconds if headline else args.cpu_seconds / 2)
            if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None)
@@ -496,7 +498,145 @@ def measure(workload, args, rank, world, dist, device, steps, warmup, headline):
 
 
 WORKLOAD_STEPS = {"tiny_decode": 400, "decode_batch": 400, "long_context_decode": 200, "prefill_chunk": 40,
-                  "prefill_chunk_paged": 40, "shared_schedule": 200}
+                  "prefill_chunk_paged": 40, "shared_schedule": 200, "multi_token_decode": 400,
+                  "candidate_source": 100, "producers": 100}
+
+
+def _time_graph(step, nrep, steps, warmup, dist, device):
+    """Warm up, capture `min(nrep, steps)` steps in a graph, time `steps` steps
+    by replaying it; returns the max-over-ranks milliseconds."""
+    import torch
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    G = min(nrep, steps)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for j in range(G):
+            step(j)
+    rem = steps % G
+    graph_rem = None
+    if rem:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem):
+            for j in range(rem):
+                step(j)
+    graph.replay()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps // G):
+        graph.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    return reduce_max(t0.elapsed_time(t1), dist, device), G
+
+
+def measure_source(args, rank, world, dist, device, steps, warmup):
+    """The candidate-source indexer on the decode batch's rows: every position
+    of each row's context scored (dense), block maxima, the 32 best blocks."""
+    import torch
+
+    import sparse_attention_top_expand_gb300 as smq
+    from sparse_attention_top_expand_gb300 import synth, tensors
+
+    inp = synth.decode_batch(seed=rank_seed(1, rank))
+    g = inp.geom
+    plan = tensors.plan_for(g, max_rows=inp.rows, device=device.index)
+    max_ctx = int(inp.row_ke.max())
+    positions = int(np.maximum(inp.row_ke, 0).sum())
+    touched = positions * 68 + inp.rows * g.num_heads * 128
+    nrep = args.replicas or max(2, min(64, math.ceil(4 * L2_BYTES / touched)))
+    reps = []
+    for _ in range(nrep):
+        d = tensors.DecodeDevice(inp, plan, with_logits=False, with_cols=False)
+        d.cand = torch.empty((inp.rows, g.candidate_topk_blocks), dtype=torch.int32, device=device)
+        d.ws = torch.empty(smq.smq_source_workspace_size(plan, inp.rows, max_ctx), dtype=torch.uint8, device=device)
+        smq.smq_workspace_init(plan, d.ws)
+        reps.append(d)
+
+    def step(i):
+        d = reps[i % nrep]
+        smq.sparse_mqa_candidate_source_decode(plan, d.q, d.q_scale, d.weights, d.k_cache, d.block_table,
+                                               d.row_indices, d.row_ke, max_ctx, d.cand, d.ws)
+
+    ms, G = _time_graph(step, nrep, steps, warmup, dist, device)
+    for d in reps:
+        st = smq.smq_get_status(d.ws)
+        if st:
+            raise SystemExit(f"candidate_source: device status {st}")
+    ms_step = ms / steps
+    nsub = int(((np.maximum(inp.row_ke, 0) + plan.sparse_block_kv - 1) // plan.sparse_block_kv).sum())
+    alg = positions * 68 + inp.rows * (g.num_heads * g.head_dim + 4 + 2 * g.num_heads + 4 * g.candidate_topk_blocks) \
+        + 4 * nsub
+    peaks, src = load_peaks()
+    achieved = alg / (ms_step / 1e3) / 1e9
+    return {"value": reduce_sum(positions * steps, dist, device) / (ms / 1e3), "unit": "positions/s",
+            "ms_per_step": ms_step, "rows_per_s": reduce_sum(inp.rows * steps, dist, device) / (ms / 1e3),
+            "config": {"workload": "candidate_source", "rows": inp.rows, "heads": g.num_heads,
+                       "positions_per_step": positions, "candidate_block_size": g.candidate_block_size,
+                       "published_blocks": g.candidate_topk_blocks, "replicas": nrep, "graph_steps": G,
+                       "contexts": "the decode batch's: uniform in [4096, 32768]"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": alg,
+                         "time": "step time: layout, dense score kernel and block selection (3 launches)"},
+            "gpu_launches": 3 * steps, "steps": steps}
+
+
+def measure_producers(args, rank, world, dist, device, steps, warmup):
+    """The device producers on a prefill chunk's sizes: 65536 bf16 keys into the
+    paged MXFP4 cache (random slots) and 4096 query rows of 64 heads to E4M3."""
+    import torch
+
+    import sparse_attention_top_expand_gb300 as smq
+
+    ntok, page, rows, H = 65536, 64, 4096, 64
+    plan = smq.Plan(num_heads=H, page_size=page, candidate_block_size=128, candidate_topk_blocks=32, topk=2048,
+                    max_rows=rows, device=device.index)
+    gen = torch.Generator(device="cpu").manual_seed(rank_seed(6, rank))
+    per = ntok * (256 + 8) + rows * H * (256 + 4)
+    nrep = args.replicas or max(2, min(64, math.ceil(4 * L2_BYTES / per)))
+    reps = []
+    for _ in range(nrep):
+        r = {"k": (torch.randn((ntok, 128), generator=gen) * 3).to(torch.bfloat16).to(device),
+             "slots": torch.randperm(ntok, generator=gen).to(torch.int64).to(device),
+             "cache": torch.zeros((ntok // page, plan.page_bytes), dtype=torch.uint8, device=device),
+             "q": torch.randn((rows, H, 128), generator=gen).to(torch.bfloat16).to(device),
+             "w": torch.randn((rows, H), generator=gen).to(device),
+             "q8": torch.empty((rows, H, 128), dtype=torch.uint8, device=device),
+             "qs": torch.empty(rows, dtype=torch.float32, device=device),
+             "wb": torch.empty((rows, H), dtype=torch.int16, device=device),
+             "ws": plan.workspace(1)}
+        reps.append(r)
+
+    def step(i):
+        r = reps[i % nrep]
+        smq.sparse_mqa_write_k_cache(plan, r["k"], r["slots"], r["cache"], r["ws"])
+        smq.sparse_mqa_quantize_q(plan, r["q"], r["w"], r["q8"], r["qs"], r["wb"])
+
+    ms, G = _time_graph(step, nrep, steps, warmup, dist, device)
+    for r in reps:
+        if smq.smq_get_status(r["ws"]):
+            raise SystemExit("producers: device status")
+    ms_step = ms / steps
+    alg = ntok * (256 + 8 + 68) + rows * (H * 128 * 2 + H * 4 + H * 128 + 4 + H * 2)
+    peaks, src = load_peaks()
+    achieved = alg / (ms_step / 1e3) / 1e9
+    return {"value": reduce_sum(ntok * steps, dist, device) / (ms / 1e3), "unit": "keys/s",
+            "q_rows_per_s": reduce_sum(rows * steps, dist, device) / (ms / 1e3), "ms_per_step": ms_step,
+            "config": {"workload": "producers", "keys_per_step": ntok, "page_size": page, "q_rows_per_step": rows,
+                       "heads": H, "replicas": nrep, "graph_steps": G},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": alg,
+                         "time": "step time: the K-cache writer and the query quantiser (2 launches)"},
+            "gpu_launches": 2 * steps, "steps": steps}
 
 
 def run_ours(args, rank, world, dist):
@@ -519,11 +659,15 @@ def run_ours(args, rank, world, dist):
     if not args.no_workloads:
         others = {}
         for w in ("tiny_decode", "long_context_decode", "prefill_chunk", "prefill_chunk_paged", "shared_schedule",
-                  "decode_batch"):
+                  "multi_token_decode", "decode_batch"):
             if w == args.workload:
                 continue
             others[w] = measure(w, args, rank, world, dist, device, WORKLOAD_STEPS[w], max(3, args.warmup),
                                 headline=False)
+        others["candidate_source"] = measure_source(args, rank, world, dist, device, WORKLOAD_STEPS["candidate_source"],
+                                                    max(3, args.warmup))
+        others["producers"] = measure_producers(args, rank, world, dist, device, WORKLOAD_STEPS["producers"],
+                                                max(3, args.warmup))
         line["workloads"] = others
     return line
 
@@ -780,7 +924,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
                     choices=["tiny_decode", "decode_batch", "long_context_decode", "prefill_chunk",
-                             "prefill_chunk_paged", "shared_schedule"])
+                             "prefill_chunk_paged", "shared_schedule", "multi_token_decode"])
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
