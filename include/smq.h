@@ -126,6 +126,20 @@ SMQ_API int smq_plan_create(const smq_plan_desc *desc, smq_plan **plan);
 SMQ_API int smq_plan_destroy(smq_plan *plan);
 SMQ_API int smq_plan_get_info(const smq_plan *plan, smq_plan_info *info);
 
+/* Failure-path controls of later calls with this plan (host side; not
+ * thread-safe with calls in flight on other threads).
+ *  - smq_plan_set_wait_limit: every pipeline wait gives up after ns
+ *    nanoseconds (default 2e9) and raises SMQ_ERR_TIMEOUT; the kernel then
+ *    winds down: it waits, bounded, for its own copies in flight, drains its
+ *    MMAs and frees its TMEM.
+ *  - smq_plan_inject_stall: for tests of that path. The loaders of the first
+ *    CTA of the score kernel withhold the hand-off of its tile `tile` to the
+ *    MMA, so that the MMA's wait runs out. -1 (the default) withholds
+ *    nothing. The outputs of a stalled call are unspecified; zero the
+ *    workspace (smq_workspace_init) before the next call. */
+SMQ_API int smq_plan_set_wait_limit(smq_plan *plan, int64_t ns);
+SMQ_API int smq_plan_inject_stall(smq_plan *plan, int32_t tile);
+
 /* Device workspace bytes for calls of up to `rows` rows (<= max_rows).
  * It holds the status word, one tile counter per plan row (decode calls that
  * expand their rows in the score kernel also select their top-k there; the
@@ -227,7 +241,7 @@ SMQ_API int sparse_mqa_logits_topk_decode(const smq_plan *plan, const smq_decode
  *  - The counters (4 bytes per plan row, rounded up to 256) plus
  *    rows * num_sparse_cols * 4 must not exceed 8 MiB, for example 200 rows
  *    of 8192 columns. A larger call returns SMQ_ERR_WORKSPACE_TOO_SMALL and
- *    enqueues nothing.
+ *    enqueues nothing. The limit holds whether or not logits_out is given.
  *  - The first call on a device looks up the scratch's device address
  *    (cudaGetSymbolAddress) with that device current. Make that first call
  *    before any stream capture.

@@ -77,7 +77,7 @@ EXPORTED = [
     "smq_get_status", "smq_error_string", "sparse_mqa_candidate_expand", "sparse_mqa_logits_topk_decode",
     "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k", "sparse_mqa_logits_topk_decode_noalloc",
     "sparse_mqa_write_k_cache", "sparse_mqa_quantize_q", "smq_source_workspace_size",
-    "sparse_mqa_candidate_source_decode",
+    "sparse_mqa_candidate_source_decode", "smq_plan_set_wait_limit", "smq_plan_inject_stall",
 ]
 
 _lib = None
@@ -109,6 +109,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_mqa_write_k_cache.argtypes = [_vp, _vp, _vp, _c_i64, _vp, _c_i64, _vp, ctypes.c_size_t, _vp]
     lib.sparse_mqa_quantize_q.argtypes = [_vp, _vp, _vp, _c_i32, _vp, _vp, _vp, _vp]
     lib.smq_source_workspace_size.argtypes = [_vp, _c_i32, _c_i32, P(ctypes.c_size_t)]
+    lib.smq_plan_set_wait_limit.argtypes = [_vp, _c_i64]
+    lib.smq_plan_inject_stall.argtypes = [_vp, _c_i32]
     lib.sparse_mqa_candidate_source_decode.argtypes = [_vp, P(SMQSourceArgs), _vp]
     for name in EXPORTED:
         if name != "smq_error_string":
@@ -198,6 +200,14 @@ class Plan:
         self.num_sparse_cols = info.num_sparse_cols
         self.page_bytes = info.page_bytes
         self.num_sms = info.num_sms
+
+    def set_wait_limit(self, ns: int) -> None:
+        """Every pipeline wait of later calls gives up after ns nanoseconds (default 2 s)."""
+        _check(load_library().smq_plan_set_wait_limit(self.handle, int(ns)), "smq_plan_set_wait_limit")
+
+    def inject_stall(self, tile: int) -> None:
+        """Failure-path tests: withhold tile `tile`'s hand-off in the first CTA (-1: none)."""
+        _check(load_library().smq_plan_inject_stall(self.handle, int(tile)), "smq_plan_inject_stall")
 
     def workspace_size(self, rows: int) -> int:
         n = ctypes.c_size_t()

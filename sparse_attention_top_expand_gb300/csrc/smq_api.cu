@@ -19,6 +19,8 @@ using smq::kTileM;
 
 struct smq_plan {
   smq_plan_desc desc;
+  int64_t wait_ns;     // every pipeline wait gives up after this (smq_plan_set_wait_limit)
+  int32_t stall_tile;  // failure-path tests: a withheld hand-off (smq_plan_inject_stall), -1: none
   int32_t sbkv;
   int32_t nsb;
   int32_t num_cols;
@@ -190,6 +192,8 @@ smq::ScoreParams score_params(const smq_plan* p, const CommonRows& a) {
   s.sparse_indices = a.sparse_indices;
   s.end = a.end;
   s.status = static_cast<int32_t*>(a.workspace);
+  s.wait_ns = p->wait_ns;
+  s.stall_tile = p->stall_tile;
   s.row_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + kStatusBytes);
   s.logits_bf16 = a.logits_out_bf16;
   s.logits = a.logits_out ? a.logits_out
@@ -338,6 +342,8 @@ SMQ_API int smq_plan_create(const smq_plan_desc* desc, smq_plan** plan) {
   p->num_sms = sms;
   p->n_mma = d.num_heads <= 64 ? 64 : 128;
   p->prepared = false;
+  p->wait_ns = 2000000000ll;  // 2 s: far beyond any legitimate wait
+  p->stall_tile = -1;
   if (!smem_fits(p, d.max_rows)) {
     delete p;
     return SMQ_ERR_UNSUPPORTED;
@@ -358,6 +364,18 @@ SMQ_API int smq_plan_get_info(const smq_plan* plan, smq_plan_info* info) {
   info->num_sparse_cols = plan->num_cols;
   info->page_bytes = plan->page_bytes;
   info->num_sms = plan->num_sms;
+  return SMQ_OK;
+}
+
+SMQ_API int smq_plan_set_wait_limit(smq_plan* plan, int64_t ns) {
+  if (!plan || ns <= 0) return SMQ_ERR_INVALID_ARG;
+  plan->wait_ns = ns;
+  return SMQ_OK;
+}
+
+SMQ_API int smq_plan_inject_stall(smq_plan* plan, int32_t tile) {
+  if (!plan || tile < -1) return SMQ_ERR_INVALID_ARG;
+  plan->stall_tile = tile;
   return SMQ_OK;
 }
 
@@ -706,6 +724,8 @@ SMQ_API int sparse_mqa_candidate_source_decode(const smq_plan* plan, const smq_s
   p.logits = const_cast<float*>(sp.logits);
   p.status = sp.status;
   p.row_done = reinterpret_cast<int32_t*>(ws + kStatusBytes);
+  p.wait_ns = plan->wait_ns;
+  p.stall_tile = plan->stall_tile;
   const int64_t tiles = static_cast<int64_t>(a.rows) * ((l.num_cols + kTileM - 1) / kTileM);
   const int grid = static_cast<int>(tiles < plan->num_sms ? tiles : plan->num_sms);
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);

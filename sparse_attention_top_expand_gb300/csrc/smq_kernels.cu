@@ -45,7 +45,6 @@ namespace smq {
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kE2M1 = 5, kE4M3 = 0;
 constexpr int32_t kRowDone = 0x40000000;  // flag on a row's end: this CTA selects the row's top-k
@@ -79,9 +78,9 @@ struct ScoreLayout {
     o += 2u * w_stride;
     meta = o;  // [2] {row, end, q_scale, unused}
     o += 2u * 16u;
-    bars = o;  // full, empty [stages]; acc_full, acc_empty [accumulators]; q_full, q_empty [2]; drain [2];
+    bars = o;  // full, empty [stages]; acc_full, acc_empty [accumulators]; q_full, q_empty [2]; drain [2]; (then, below)
                // desc_full, desc_empty [ring]; setup copy; row stored
-    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing + 2u) * 8u, 16);
+    o += round_up((2u * kScoreStages + 2u * kMaxAccBuffers + 6u + 2u * kDescRing + 2u + kScoreStages) * 8u, 16);
     misc = o;  // tmem base, abort flag
     o += 16u;
     scan = o;  // per-warp partial sums of the prologue scan
@@ -645,6 +644,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   auto bar_desc_empty = [&](int d) { return smem_addr(&bars[NB + 6 + kDescRing + d]); };
   const uint32_t bar_setup = smem_addr(&bars[NB + 6 + 2 * kDescRing]);
   const uint32_t bar_row_stored = smem_addr(&bars[NB + 7 + 2 * kDescRing]);  // epilogue warps, per row end
+  // tensor-copy path: the value copies of a stage complete here (the `full`
+  // barrier then counts the loader warps' scale words only)
+  auto bar_copy = [&](int st) { return smem_addr(&bars[NB + 8 + 2 * kDescRing + st]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.misc + 4);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + lay.scan);
@@ -656,8 +658,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       // one arrival per loader warp, and (tensor-copy path) the value copies' expect
-      mbar_init(bar_full(s), kLoaderThreads / 32 + (kCopy ? 1 : 0));
+      mbar_init(bar_full(s), kLoaderThreads / 32);
       mbar_init(bar_empty(s), 1);
+      if (kCopy) mbar_init(bar_copy(s), 1);  // warp 6's expected bytes
     }
     for (int d = 0; d < kDescRing; ++d) {
       mbar_init(bar_desc_full(d), 1);
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (tid == 32) {
     tmem_cp_32x128b_x4(tm_sfb, rows16_desc(smem_addr(sf_one)));
     mma_commit(bar_setup);
-    if (!mbar_wait(bar_setup, 0, abort_flag, kWaitLimitNs)) {
+    if (!mbar_wait(bar_setup, 0, abort_flag, static_cast<uint64_t>(p.wait_ns))) {
       set_status(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
@@ -836,7 +839,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int dslot = it % kDescRing;
           bool e_ok = true;
           if (lane == 0)
-            e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           if (lane >= base && lane < base + spt) put_src(&desc[dslot * kMaxSubsPerTile + (lane - base)], vsrc, ssrc, trow, tpage, ntok);
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int dslot = it % kDescRing;
         bool e_ok = true;
         if (lane == 0)
-          e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // the lanes that resolved this tile's sub-blocks publish them
@@ -954,7 +957,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (r == cur) continue;
         cur = r;
         const int qb = quse & 1;
-        ok = mbar_wait(bar_q_empty(qb), ((quse >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        ok = mbar_wait(bar_q_empty(qb), ((quse >> 1) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         if (!ok) break;
         meta[qb].row = r;
         if constexpr (!kFused) {  // expanded rows' ends come from the scheduler
@@ -976,7 +979,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // the last query load must land before the CTA exits (it has, unless a wait gave up)
       if (quse > 0) {
         const volatile int never = 0;
-        mbar_wait(bar_q_full((quse - 1) & 1), ((quse - 1) >> 1) & 1, &never, kWaitLimitNs);
+        mbar_wait(bar_q_full((quse - 1) & 1), ((quse - 1) >> 1) & 1, &never, static_cast<uint64_t>(p.wait_ns));
       }
     }
     __syncwarp();
@@ -1004,7 +1007,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ++quse;
           // both threads wait for every row's query, so that neither can skip a
           // phase of a buffer and later match its parity too early
-          ok = mbar_wait(bar_q_full(qb), ((quse - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+          ok = mbar_wait(bar_q_full(qb), ((quse - 1) >> 1) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
         }
         const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
@@ -1012,8 +1015,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (NA > 1 ? ((it & 1) == par) : (par == 0)) {
           const int s = it % NS;
           const int a = it % NA;
-          ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
-               mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns)) &&
+               (!kCopy || mbar_wait(bar_copy(s), (it / NS) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns))) &&
+               mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
           tc_fence_after();
           const uint32_t stage_addr = smem_addr(smem + lay.kv + s * (kTileM * kRowBytes));
@@ -1040,7 +1044,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint32_t drain = bar_drain + 8 * par;
       mma_commit(drain);  // every MMA this thread issued has finished once this arrives
       const volatile int never = 0;
-      mbar_wait(drain, 0, &never, kWaitLimitNs);
+      mbar_wait(drain, 0, &never, static_cast<uint64_t>(p.wait_ns));
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -1075,7 +1079,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         need_end = kFused;
         cur = r;
         qb = quse & 1;
-        ok = warp_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, kWaitLimitNs);
+        ok = warp_wait(bar_q_full(qb), (quse >> 1) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         ++quse;
         if (!ok) break;
         row = meta[qb].row;
@@ -1087,7 +1091,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
       const int a = ie % NA;
-      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
+      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
       if (!ok) break;
       if (need_end) {  // written by the scheduler before it published this row's first tile
         e = ld_volatile_s32(reinterpret_cast<const int32_t*>(smem + lay.rend) + (r - r_first)) & ~kRowDone;
@@ -1138,7 +1142,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             // completes the row selects its top-k after the pipeline
             if (lane == 0) mbar_arrive(bar_row_stored);
             if (warp == 2 && lane == 0) {
-              if (mbar_wait(bar_row_stored, nrow_ends & 1, abort_flag, kWaitLimitNs)) {
+              if (mbar_wait(bar_row_stored, nrow_ends & 1, abort_flag, static_cast<uint64_t>(p.wait_ns))) {
                 const int64_t lo = prefix[r] > t_begin ? prefix[r] : t_begin;
                 const int64_t hi = prefix[r + 1] < t_end ? prefix[r + 1] : t_end;
                 const int mine = static_cast<int>(hi - lo), total = prefix[r + 1] - prefix[r];
@@ -1230,7 +1234,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
         fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
         __syncwarp();              // one arrival per warp
-        if (lane == 0) mbar_arrive(bar_full(s));
+        if (lane == 0 && !(j == p.stall_tile && blockIdx.x == 0)) mbar_arrive(bar_full(s));
         if (warp == 6 && lane == 0 && j == 0) SMQ_MARK(7);
         if (warp == 6 && lane == 0 && j == n - 1) SMQ_MARK(8);
       };
@@ -1256,7 +1260,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (j0 >= 0 && j0 < n) {
           const int jl = j0 + 1 < n ? j0 + 1 : j0;
           // the stages are free once the MMAs of tiles j0 - NS and jl - NS have finished
-          ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+          ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
           store_tile(v[0], sw[0], j0);
           if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
@@ -1271,13 +1275,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
           __syncwarp();  // orders the other lanes after lane 0's acquire
           if (!both) {
-            ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
             if (!ok) break;
           }
           load_tile(v[0], sw[0], i0);
           if (i0 + 1 < n) {
             if (!both) {
-              ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+              ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
               if (!ok) break;
             }
             load_tile(v[1], sw[1], i0 + 1);
@@ -1315,6 +1319,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         stk[h] = (m + h * kMmaM) % sbkv;
       }
       uint32_t sw[2][kHalves];
+      int issued = 0;  // (warp 6) tiles whose value copies are out
       for (int i0 = 0; i0 < n + 2 && ok; i0 += 2) {
   #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -1328,11 +1333,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, sw[k][h]);
             fence_proxy_async_smem();  // make this thread's stores visible to the tensor core's reads
             __syncwarp();              // one arrival per warp
-            if (lane == 0) mbar_arrive(bar_full(s));
+            if (lane == 0 && !(j == p.stall_tile && blockIdx.x == 0)) mbar_arrive(bar_full(s));
           }
           if (i < n) {
             const int dslot = i % kDescRing;
-            ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            ok = warp_wait(bar_desc_full(dslot), (i / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
             if (!ok) break;
             const SubBlockSrc* dring = desc + dslot * kMaxSubsPerTile;
   #pragma unroll
@@ -1349,29 +1354,33 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(bar_desc_empty(dslot));
             // the stage is free once the MMAs of tile i - NS have finished
             const int s = i % NS;
-            ok = warp_wait(bar_empty(s), ((i / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            ok = warp_wait(bar_empty(s), ((i / NS) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
             if (!ok) break;
             if (warp == 6) {
               const bool live = copier && dv.positions > 0;
               const uint32_t nlive = __popc(__ballot_sync(kFullMask, live));
-              if (lane == 0) mbar_arrive_expect_tx(bar_full(s), nlive * sub_tx);
+              if (lane == 0) mbar_arrive_expect_tx(bar_copy(s), nlive * sub_tx);
               if (live) tma_load_3d(kv_base + s * (kTileM * kRowBytes) + lane * sub_bytes, &tm_k, 0, dv.row, dv.page,
-                                    bar_full(s));
+                                    bar_copy(s));
+              issued = i + 1;
             }
           }
         }
       }
+      if (warp == 6 && lane == 0) {
+        // the copies of the last NS tiles may still be in flight (each earlier
+        // stage was reused, so its copies had landed), also when a wait of
+        // another warp gives up later: wait, bounded, for them before the CTA
+        // and its shared memory can go away
+        const volatile int never = 0;
+        for (int t = issued > NS ? issued - NS : 0; t < issued; ++t)
+          mbar_wait(bar_copy(t % NS), (t / NS) & 1, &never, static_cast<uint64_t>(p.wait_ns));
+      }
+      __syncwarp();
     }
     if (!ok) {
       set_status(p.status, kStatusTimeout);
       *abort_flag = 1;
-    }
-    if (kCopy && warp == 6 && *abort_flag != 0) {
-      // value copies already issued land within microseconds; let them finish
-      // before the CTA (and its shared memory) can go away
-      const uint64_t t0 = global_ns();
-      while (global_ns() - t0 < 20000u) {
-      }
     }
   }
 
@@ -1668,7 +1677,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (tid == 32) {
       tmem_cp_32x128b_x4(tmem + NA * kHalves * kN + 4 * kHalves * NS, rows16_desc(smem_addr(sf_one)));
       mma_commit(bar_setup);
-      if (!mbar_wait(bar_setup, 0, abort_flag, kWaitLimitNs)) {
+      if (!mbar_wait(bar_setup, 0, abort_flag, static_cast<uint64_t>(p.wait_ns))) {
         set_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
@@ -1754,7 +1763,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int base = k * spt;
         const int dslot = it % kDescRing;
         bool e_ok = true;
-        if (lane == 0) e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (lane == 0) e_ok = mbar_wait(bar_desc_empty(dslot), ((it / kDescRing) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         ok = __shfl_sync(kFullMask, e_ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         if (lane >= base && lane < base + spt)
@@ -1784,7 +1793,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tma_load_2d(smem_addr(smem + lay.q), &tm_q, 0, r * H, bar_q_full);
       bulk_load(smem_addr(smem + lay.w), p.weights + static_cast<int64_t>(r) * H, H * 2, bar_q_full);
       const volatile int never = 0;
-      mbar_wait(bar_q_full, 0, &never, kWaitLimitNs);  // the copies land before the CTA can exit
+      mbar_wait(bar_q_full, 0, &never, static_cast<uint64_t>(p.wait_ns));  // the copies land before the CTA can exit
     }
     __syncwarp();
   } else if (warp == 1 || warp == kMmaWarp1) {
@@ -1793,14 +1802,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (lane == 0 && n > 0) {
       uint32_t idesc[4];
       for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kMmaM, kN, g, g);
-      bool ok = mbar_wait(bar_q_full, 0, abort_flag, kWaitLimitNs);
+      bool ok = mbar_wait(bar_q_full, 0, abort_flag, static_cast<uint64_t>(p.wait_ns));
       const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q));
       for (int it = 0; it < n && ok; ++it) {
         if (NA > 1 ? ((it & 1) != par) : (par != 0)) continue;
         const int s = it % NS;
         const int a = it % NA;
-        ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, kWaitLimitNs) &&
-             mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        ok = mbar_wait(bar_full(s), (it / NS) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns)) &&
+             mbar_wait(bar_acc_empty(a), ((it / NA) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         if (!ok) break;
         tc_fence_after();
         const uint32_t stage_addr = smem_addr(smem + lay.kv + s * (kTileM * kRowBytes));
@@ -1822,7 +1831,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint32_t drain = bar_drain + 8 * par;
       mma_commit(drain);
       const volatile int never = 0;
-      mbar_wait(drain, 0, &never, kWaitLimitNs);
+      mbar_wait(drain, 0, &never, static_cast<uint64_t>(p.wait_ns));
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -1833,7 +1842,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int q4 = warp & 3;
     const int m = 32 * q4 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    bool ok = n > 0 ? warp_wait(bar_q_full, 0, abort_flag, kWaitLimitNs) : true;
+    bool ok = n > 0 ? warp_wait(bar_q_full, 0, abort_flag, static_cast<uint64_t>(p.wait_ns)) : true;
     float w[kN];
     const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w);
 #pragma unroll
@@ -1844,7 +1853,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     int e = 0;
     for (int ie = 0; ie < n && ok; ++ie) {
       const int a = ie % NA;
-      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, kWaitLimitNs);
+      ok = warp_wait(bar_acc_full(a), (ie / NA) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
       if (!ok) break;
       if (ie == 0) e = ld_volatile_s32(end_sm);  // written before the first tile was published
       if (warp == 2 && lane == 0) mbar_arrive(bar_empty(ie % NS));
@@ -1929,7 +1938,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int h = 0; h < kHalves; ++h) sts_u32(sf_base + (s * kHalves + h) * 512 + 16 * lane + 4 * q4, ss[h]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full(s));
+      if (lane == 0 && !(j == p.stall_tile && blockIdx.x == 0)) mbar_arrive(bar_full(s));
       if (warp == 6 && lane == 0 && j == 0) SMQ_MARK(7);
       if (warp == 6 && lane == 0 && j == n - 1) SMQ_MARK(8);
     };
@@ -1954,7 +1963,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int j0 = i0 - 2;
       if (j0 >= 0 && j0 < n) {
         const int jl = j0 + 1 < n ? j0 + 1 : j0;
-        ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
         if (!ok) break;
         store_tile(v[0], sw[0], j0);
         if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
@@ -1966,13 +1975,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
         __syncwarp();
         if (!both) {
-          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, kWaitLimitNs);
+          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
         }
         load_tile(v[0], sw[0], i0);
         if (i0 + 1 < n) {
           if (!both) {
-            ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, kWaitLimitNs);
+            ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
             if (!ok) break;
           }
           load_tile(v[1], sw[1], i0 + 1);
@@ -2052,7 +2061,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   sm.chunk = reinterpret_cast<uint32_t*>(sm.wsum + 32);
   sm.sel = reinterpret_cast<int*>(sm.chunk + 32 * 32);
   sm.sidx = sidx;
-  if (!warp_wait(bar_recv(0), 0, abort_flag, kWaitLimitNs)) set_status(p.status, kStatusTimeout);
+  if (!warp_wait(bar_recv(0), 0, abort_flag, static_cast<uint64_t>(p.wait_ns))) set_status(p.status, kStatusTimeout);
   if (tid == 0) SMQ_MARK(14);
   select_topk<kScoreThreads, kJ, true, true>(lg, S, end_sm, k, nullptr, p.nsb, sbkv, out, colo, nullptr, nullptr, sm);
   if (tid == 0) SMQ_MARK(16);

@@ -118,6 +118,11 @@ struct ScoreParams {
   // outputs
   float* logits;     // [rows][num_cols]
   int32_t* status;   // workspace status word
+  // failure path: every wait gives up after wait_ns; with stall_tile >= 0 the
+  // loaders of CTA 0 withhold the hand-off of that tile (counted in CTA 0) to
+  // the MMA, whose wait then runs out (tests of the failure path only)
+  int64_t wait_ns;
+  int32_t stall_tile;
 };
 
 struct TopkParams {

@@ -70,26 +70,40 @@ def test_noalloc_matches_workspace_entry_point_twice():
     assert torch.equal(again.topk_out, ref.topk_out) and torch.equal(again.col_indices, ref.col_indices)
 
 
-def test_noalloc_rejects_more_logits_than_its_scratch():
-    inp = synth.decode_batch(rows=2)  # 4096 sparse columns: 513 rows overflow 8 MiB
+def test_noalloc_takes_exactly_what_its_scratch_holds():
+    """The scratch holds the tile counters (4 bytes per plan row, rounded up to
+    256) and rows x sparse columns x 4 bytes of logits. The largest row count
+    that fits runs; one more row is refused and enqueues nothing."""
+    inp = synth.decode_batch(rows=2)  # 4096 sparse columns
     plan = tensors.plan_for(inp.geom, max_rows=1024)
-    rows = smq.SMQ_NOALLOC_SCRATCH_BYTES // (4 * plan.num_sparse_cols) + 1
-    assert rows == 513
+    counters = (4 * plan.max_rows + 255) // 256 * 256
+    fit = (smq.SMQ_NOALLOC_SCRATCH_BYTES - counters) // (4 * plan.num_sparse_cols)
+    assert fit == 511
     dev = plan.device
     H, D = inp.geom.num_heads, inp.geom.head_dim
-    q = torch.zeros((rows, H, D), dtype=torch.uint8, device=dev)
-    qs = torch.ones(rows, dtype=torch.float32, device=dev)
-    w = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
+
+    def buffers(rows):
+        q = torch.zeros((rows, H, D), dtype=torch.uint8, device=dev)
+        qs = torch.ones(rows, dtype=torch.float32, device=dev)
+        w = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
+        ri = torch.zeros(rows, dtype=torch.int32, device=dev)
+        ke = torch.ones(rows, dtype=torch.int32, device=dev)  # one position per row
+        cand = torch.zeros((rows, plan.candidate_topk_blocks), dtype=torch.int32, device=dev)
+        top = torch.full((rows, plan.topk), -7, dtype=torch.int32, device=dev)
+        si = torch.full((rows, plan.num_sparse_blocks), -7, dtype=torch.int32, device=dev)
+        end = torch.full((rows,), -7, dtype=torch.int32, device=dev)
+        return q, qs, w, ri, ke, cand, top, si, end
+
     kc = torch.from_numpy(np.ascontiguousarray(inp.k_cache)).to(dev)
     bt = torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev)
-    ri = torch.zeros(rows, dtype=torch.int32, device=dev)
-    ke = torch.ones(rows, dtype=torch.int32, device=dev)
-    cand = torch.zeros((rows, plan.candidate_topk_blocks), dtype=torch.int32, device=dev)
-    top = torch.full((rows, plan.topk), -7, dtype=torch.int32, device=dev)
-    si = torch.full((rows, plan.num_sparse_blocks), -7, dtype=torch.int32, device=dev)
-    end = torch.full((rows,), -7, dtype=torch.int32, device=dev)
+    q, qs, w, ri, ke, cand, top, si, end = buffers(fit)
+    smq.sparse_mqa_logits_topk_decode_noalloc(plan, q, qs, w, kc, bt, ri, ke, cand, top, si, end)
+    torch.cuda.synchronize()
+    assert int((end == 1).sum()) == fit, "every row has its one position"
+    assert bool((top[:, 0] == 0).all()) and bool((top[:, 1:] == -1).all()), "token 0, then -1"
+    q, qs, w, ri, ke, cand, top, si, end = buffers(fit + 1)
     with pytest.raises(smq.SMQError) as e:
         smq.sparse_mqa_logits_topk_decode_noalloc(plan, q, qs, w, kc, bt, ri, ke, cand, top, si, end)
     assert e.value.code == smq.SMQ_ERR_WORKSPACE_TOO_SMALL
     torch.cuda.synchronize()
-    assert int((top == -7).sum()) == top.numel() and int((end == -7).sum()) == rows
+    assert int((top == -7).sum()) == top.numel() and int((end == -7).sum()) == fit + 1
