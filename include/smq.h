@@ -149,6 +149,19 @@ SMQ_API int smq_plan_inject_stall(smq_plan *plan, int32_t tile);
  * zero the workspace again before the next call. */
 SMQ_API int smq_workspace_size(const smq_plan *plan, int32_t rows, size_t *bytes);
 
+/* Device workspace bytes for prefill chunks of up to `rows` rows and
+ * `total_len` workspace rows. It adds to smq_workspace_size(plan, rows) the
+ * scratch of the window-major prefill path: per workspace position a window
+ * count and a cursor (int32 each), per row a record count and its 64 head
+ * weights and q_scale as float, per (row, window) pair a record (8 bytes) and
+ * a group slot (32 bytes per two records). The path applies to 64-head plans
+ * and total_len <= 2^20; otherwise the size equals smq_workspace_size.
+ * A prefill call whose workspace is smaller than this (but at least
+ * smq_workspace_size) runs the row-major path instead; both give the same
+ * logits, bit for bit, and the same top-k. Errors: SMQ_ERR_INVALID_ARG for a
+ * null plan or bytes, rows < 0 or > max_rows, total_len < 0. */
+SMQ_API int smq_prefill_workspace_size(const smq_plan *plan, int32_t rows, int64_t total_len, size_t *bytes);
+
 /* Zero the workspace status word and tile counters (async on stream). */
 SMQ_API int smq_workspace_init(const smq_plan *plan, void *workspace, size_t workspace_bytes,
                                void *stream);
@@ -260,7 +273,14 @@ SMQ_API int sparse_mqa_logits_topk_decode_noalloc(const smq_plan *plan, const sm
  * docs, SparseMQAIndexer.forward, the sparse_mqa_logits_prefill_chunk call
  * with cu_seqlen_ks / cu_seqlen_ke.) Row r's keys are workspace rows
  * [cu_seqlen_ks[r], cu_seqlen_ke[r]). Its candidate blocks and output ids
- * are relative to cu_seqlen_ks[r]. */
+ * are relative to cu_seqlen_ks[r].
+ * With a workspace of smq_prefill_workspace_size(plan, R, total_len) bytes
+ * (64-head plans) the chunk runs window-major: the rows are indexed by the
+ * 128-key windows [ks + 128 u, ks + 128 u + 128) their sparse sub-blocks fall
+ * in, and each window's keys stay in shared memory while the query tiles of
+ * the rows that selected it stream past. Four kernels then run before the
+ * top-k: record, plan and fill of the index, and the score (plus one memset
+ * of the window counts); profile_events[1] is recorded after the index. */
 typedef struct smq_prefill_args {
   uint32_t struct_size;
   int32_t rows;

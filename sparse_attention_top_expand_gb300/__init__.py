@@ -74,6 +74,7 @@ class SMQSourceArgs(ctypes.Structure):
 
 EXPORTED = [
     "smq_plan_create", "smq_plan_destroy", "smq_plan_get_info", "smq_workspace_size", "smq_workspace_init",
+    "smq_prefill_workspace_size",
     "smq_get_status", "smq_error_string", "sparse_mqa_candidate_expand", "sparse_mqa_logits_topk_decode",
     "sparse_mqa_logits_topk_prefill_chunk", "sparse_mqa_gather_k", "sparse_mqa_logits_topk_decode_noalloc",
     "sparse_mqa_write_k_cache", "sparse_mqa_quantize_q", "smq_source_workspace_size",
@@ -96,6 +97,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.smq_plan_destroy.argtypes = [_vp]
     lib.smq_plan_get_info.argtypes = [_vp, P(SMQPlanInfo)]
     lib.smq_workspace_size.argtypes = [_vp, _c_i32, P(ctypes.c_size_t)]
+    lib.smq_prefill_workspace_size.argtypes = [_vp, _c_i32, ctypes.c_int64, P(ctypes.c_size_t)]
     lib.smq_workspace_init.argtypes = [_vp, _vp, ctypes.c_size_t, _vp]
     lib.smq_get_status.argtypes = [_vp, _vp, P(_c_i32)]
     lib.smq_error_string.argtypes = [ctypes.c_int]
@@ -214,10 +216,18 @@ class Plan:
         _check(load_library().smq_workspace_size(self.handle, rows, ctypes.byref(n)), "smq_workspace_size")
         return n.value
 
-    def workspace(self, rows: Optional[int] = None, stream=None) -> torch.Tensor:
-        """Allocate (here, by torch) and zero a workspace for calls of up to `rows` rows."""
+    def prefill_workspace_size(self, rows: int, total_len: int) -> int:
+        n = ctypes.c_size_t()
+        _check(load_library().smq_prefill_workspace_size(self.handle, rows, total_len, ctypes.byref(n)),
+               "smq_prefill_workspace_size")
+        return n.value
+
+    def workspace(self, rows: Optional[int] = None, stream=None, total_len: Optional[int] = None) -> torch.Tensor:
+        """Allocate (here, by torch) and zero a workspace for calls of up to `rows` rows; with `total_len`, one
+        that also holds the window-major prefill scratch for chunks of up to that many workspace rows."""
         rows = self.max_rows if rows is None else rows
-        ws = torch.empty(self.workspace_size(rows), dtype=torch.uint8, device=self.device)
+        n = self.workspace_size(rows) if total_len is None else self.prefill_workspace_size(rows, total_len)
+        ws = torch.empty(n, dtype=torch.uint8, device=self.device)
         smq_workspace_init(self, ws, stream)
         return ws
 

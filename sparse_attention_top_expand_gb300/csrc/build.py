@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsmq.so")
 TRACE_LIB = os.path.join(PKG, "libsmq_trace.so")  # -DSMQ_TRACE: phase timestamps (include/smq_trace.h)
-SOURCES = ["smq_api.cu", "smq_kernels.cu", "smq_producers.cu"]
+SOURCES = ["smq_api.cu", "smq_kernels.cu", "smq_producers.cu", "smq_prefill.cu"]
 HEADERS = ["smq_kernels.cuh", "smq_ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -107,7 +107,8 @@ int check_device(smq_plan* p) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SMQ_ERR_CUDA;
   if (dev != p->desc.device) return SMQ_ERR_INVALID_ARG;
   if (!p->prepared) {
-    if (smq::prepare_kernels(p->n_mma) != cudaSuccess) return SMQ_ERR_CUDA;
+    if (smq::prepare_kernels(p->n_mma) != cudaSuccess || smq::prepare_bm_kernels() != cudaSuccess)
+      return SMQ_ERR_CUDA;
     p->prepared = true;
   }
   return SMQ_OK;
@@ -248,6 +249,35 @@ int row_cluster_size(const smq_plan* p, int rows) {
   return c > tiles ? tiles : c;  // a CTA without a tile would only wait
 }
 
+// Window-major prefill scratch, after the common part of the workspace:
+// per-position window counts and cursors, then per-row record counts, the
+// group count, the (row, window) records, the rows' float params and the
+// groups (at most one per record).
+struct BmScratch {
+  size_t cnt, cursor, nrec, ngroups, rec, rowparams, groups, end;
+};
+
+BmScratch bm_scratch(const smq_plan* p, int64_t rows, int64_t total_len) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t records = static_cast<size_t>(rows) * p->nsb;
+  BmScratch w;
+  w.cnt = up(workspace_bytes_for(p, rows));
+  w.cursor = w.cnt + up(static_cast<size_t>(total_len) * 4);
+  w.nrec = w.cursor + up(static_cast<size_t>(total_len) * 4);
+  w.ngroups = w.nrec + up(static_cast<size_t>(rows) * 4);
+  w.rec = w.ngroups + 256;
+  w.rowparams = w.rec + up(records * 8);
+  w.groups = w.rowparams + up(static_cast<size_t>(rows) * smq::kBmRowParams * 4);
+  w.end = w.groups + up(records * sizeof(smq::BmGroup));
+  return w;
+}
+
+// The window-major prefill path: 64 heads (two rows per MMA of N = 128) and
+// a workspace short enough to count windows per position.
+bool bm_applies(const smq_plan* p, int64_t total_len) {
+  return p->desc.num_heads == 64 && total_len > 0 && total_len <= smq::kBmMaxTotalLen;
+}
+
 int score_grid(const smq_plan* p, int rows) {
   const int64_t max_tiles = static_cast<int64_t>(rows) * ((p->num_cols + kTileM - 1) / kTileM);
   return static_cast<int>(max_tiles < p->num_sms ? max_tiles : p->num_sms);
@@ -382,6 +412,12 @@ SMQ_API int smq_plan_inject_stall(smq_plan* plan, int32_t tile) {
 SMQ_API int smq_workspace_size(const smq_plan* plan, int32_t rows, size_t* bytes) {
   if (!plan || !bytes || rows < 0 || rows > plan->desc.max_rows) return SMQ_ERR_INVALID_ARG;
   *bytes = workspace_bytes_for(plan, rows);
+  return SMQ_OK;
+}
+
+SMQ_API int smq_prefill_workspace_size(const smq_plan* plan, int32_t rows, int64_t total_len, size_t* bytes) {
+  if (!plan || !bytes || rows < 0 || rows > plan->desc.max_rows || total_len < 0) return SMQ_ERR_INVALID_ARG;
+  *bytes = bm_applies(plan, total_len) ? bm_scratch(plan, rows, total_len).end : workspace_bytes_for(plan, rows);
   return SMQ_OK;
 }
 
@@ -542,23 +578,70 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
   rc = check_device(const_cast<smq_plan*>(plan));
   if (rc != SMQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
+  const bool window_major =
+      bm_applies(plan, a.total_len) && a.workspace_bytes >= bm_scratch(plan, a.rows, a.total_len).end;
+  if (!window_major && !smem_fits(plan, a.rows)) return SMQ_ERR_UNSUPPORTED;
   CUtensorMap tm_q, tm_k;
   rc = encode_q(&tm_q, a.q, static_cast<int64_t>(a.rows) * plan->desc.num_heads, plan->n_mma);
   if (rc != SMQ_OK) return rc;
-  rc = encode_k(&tm_k, a.k_values, a.total_len, a.total_len * (kHeadDim / 2), 1, plan->sbkv);
+  // key tiles: 128-row windows (window-major) or one sub-block per copy
+  rc = encode_k(&tm_k, a.k_values, a.total_len, a.total_len * (kHeadDim / 2), 1, window_major ? 128 : plan->sbkv);
   if (rc != SMQ_OK) return rc;
   record(a.profile_events[0], s);
   if (!a.expansion_ready) {
     rc = run_expand(plan, a.candidate_blocks, a.cu_seqlen_ks, a.cu_seqlen_ke, a.rows, a.sparse_indices, a.end, s);
     if (rc != SMQ_OK) return rc;
   }
-  record(a.profile_events[1], s);
   smq::ScoreParams sp = score_params(plan, c);
   sp.row_ks = a.cu_seqlen_ks;
   sp.k_values = a.k_values;
   sp.k_scales = a.k_scales;
   sp.total_len = a.total_len;
+  if (window_major) {
+    // the (row, window) index, then the score per window
+    const BmScratch w = bm_scratch(plan, a.rows, a.total_len);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    smq::BmIndexParams ip;
+    ip.rows = a.rows;
+    ip.nsb = plan->nsb;
+    ip.sbkv = plan->sbkv;
+    ip.num_cols = plan->num_cols;
+    ip.total_len = a.total_len;
+    ip.sparse_indices = a.sparse_indices;
+    ip.end = a.end;
+    ip.row_ks = a.cu_seqlen_ks;
+    ip.weights = a.weights;
+    ip.q_scale = a.q_scale;
+    ip.rec = reinterpret_cast<int2*>(ws + w.rec);
+    ip.nrec = reinterpret_cast<int32_t*>(ws + w.nrec);
+    ip.cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+    ip.cursor = reinterpret_cast<int32_t*>(ws + w.cursor);
+    ip.rowparams = reinterpret_cast<float*>(ws + w.rowparams);
+    ip.groups = reinterpret_cast<smq::BmGroup*>(ws + w.groups);
+    ip.ngroups = reinterpret_cast<int32_t*>(ws + w.ngroups);
+    ip.status = sp.status;
+    if (smq::launch_bm_index(ip, s) != cudaSuccess) return SMQ_ERR_CUDA;
+    record(a.profile_events[1], s);
+    smq::BmScoreParams bp;
+    bp.groups = ip.groups;
+    bp.ngroups = ip.ngroups;
+    bp.rowparams = ip.rowparams;
+    bp.k_scales = a.k_scales;
+    bp.total_len = a.total_len;
+    bp.num_cols = plan->num_cols;
+    bp.sbkv = plan->sbkv;
+    bp.logits = sp.logits;
+    bp.logits_bf16 = a.logits_out_bf16;
+    bp.status = sp.status;
+    bp.wait_ns = static_cast<uint64_t>(plan->wait_ns);
+    bp.stall_group = plan->stall_tile;
+    if (smq::launch_bm_score(bp, tm_q, tm_k, plan->num_sms, s) != cudaSuccess) return SMQ_ERR_CUDA;
+    record(a.profile_events[2], s);
+    rc = run_topk(plan, c, sp, s);
+    record(a.profile_events[3], s);
+    return rc;
+  }
+  record(a.profile_events[1], s);
   const size_t smem = smq::score_smem_bytes(plan->n_mma, plan->desc.num_heads, a.rows);
   if (smq::launch_score(sp, false, true, tm_q, tm_k, score_grid(plan, a.rows), smem, s) != cudaSuccess) return SMQ_ERR_CUDA;
   record(a.profile_events[2], s);

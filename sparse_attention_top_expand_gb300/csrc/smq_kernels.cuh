@@ -238,4 +238,76 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once per device
 
+// ---------------------------------------------------------------------------
+// Window-major prefill (smq_prefill.cu). Rows of a chunk select the same key
+// windows many times over, so the score runs per 128-key window of the
+// contiguous workspace: the window's keys stay in shared memory while the
+// query tiles of the rows that selected it stream past, two rows per MMA
+// (N = 128). A window is the 128 positions from P = ks + 128 u (u >= 0) of a
+// row's own coordinates, so a sub-block never straddles two windows.
+//
+// A record is one (row, window) pair: a run of consecutive entries of the
+// row's sparse list inside one window with ascending slots (slot = offset in
+// the window / sbkv). It holds P and the column of its first entry c0, with
+// the slot mask in the top byte (c0m = c0 | mask << 24); the column of key m
+// of the window (slot s = m / sbkv, present when mask bit s is set) is
+// c0 + popc(mask & ((1 << s) - 1)) * sbkv + m % sbkv.
+// A group is two records of the same window (row[1] = -1 when the window's
+// record count is odd); groups are numbered window by window.
+constexpr int kBmThreads = 512;           // stager, 3 MMA issuers, 3 x 4 epilogue warps
+constexpr int kBmStages = 9;              // query stages of two rows (16 KB each), 3 per MMA issuer
+constexpr int kBmRowParams = 68;          // floats per row: 64 head weights, q_scale, 3 pad
+constexpr int64_t kBmMaxTotalLen = 1 << 20;  // windows are counted per workspace position
+
+struct BmGroup {
+  int32_t P;        // first workspace position of the window
+  int32_t row[2];   // row of each column half; row[1] = -1 for a lone record
+  int32_t c0m[2];   // column of the record's first entry | slot mask << 24
+  int32_t end[2];   // the row's valid column count
+  int32_t pad;
+};
+static_assert(sizeof(BmGroup) == 32, "one group descriptor is 32 bytes (a bulk copy unit)");
+
+struct BmIndexParams {
+  int rows;
+  int nsb;
+  int sbkv;
+  int num_cols;  // S
+  int64_t total_len;
+  const int32_t* sparse_indices;  // [rows][nsb]
+  const int32_t* end;             // [rows]
+  const int32_t* row_ks;          // [rows]
+  const uint16_t* weights;        // [rows][64] bf16
+  const float* q_scale;           // [rows]
+  int2* rec;                      // [rows][nsb] (P, c0m)
+  int32_t* nrec;                  // [rows]
+  int32_t* cnt;                   // [total_len], zero on entry
+  int32_t* cursor;                // [total_len]
+  float* rowparams;               // [rows][kBmRowParams]
+  BmGroup* groups;                // [rows * nsb]
+  int32_t* ngroups;               // [1]
+  int32_t* status;
+};
+
+struct BmScoreParams {
+  const BmGroup* groups;
+  const int32_t* ngroups;
+  const float* rowparams;
+  const uint8_t* k_scales;  // [total_len][4]
+  int64_t total_len;
+  int num_cols;
+  int sbkv;
+  float* logits;            // [rows][S]
+  uint16_t* logits_bf16;    // optional copy
+  int32_t* status;
+  uint64_t wait_ns;
+  int32_t stall_group;      // failure-path tests: CTA 0 withholds this group's stage, -1: none
+};
+
+size_t bm_score_smem_bytes();
+cudaError_t launch_bm_index(const BmIndexParams& p, cudaStream_t stream);  // zeroes cnt, then 3 kernels
+cudaError_t launch_bm_score(const BmScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kw, int grid,
+                            cudaStream_t stream);
+cudaError_t prepare_bm_kernels();
+
 }  // namespace smq

@@ -1,0 +1,681 @@
+// Window-major prefill scoring for sm_103a.
+//
+// The rows of a prefill chunk draw their candidate blocks from the same
+// sequences, so each 128-key window of the gathered workspace is selected by
+// many rows. Here the score runs per window: the window's keys (E2M1 values
+// unpacked into the MMA's 16-byte containers, UE8M0 scale words) are loaded
+// into shared memory once and stay there, and the E4M3 query tiles of the rows
+// that selected it stream past, two rows per block-scaled MMA (N = 128, the
+// full rate of tcgen05.mma kind::mxf8f6f4). The logits are the same as the
+// row-major score kernel's, bit for bit: q_scale * sum_h w_h * max(q_h . k, 0)
+// with the same accumulation order, written to the row's sparse column.
+//
+//   bm_records_kernel  one warp per row: the row's (row, window) records, the
+//                      per-window record counts, the row's float weights
+//   bm_plan_kernel     one CTA: groups of two records per window, numbered
+//                      window by window (an exclusive scan over positions)
+//   bm_fill_kernel     one warp per row: each record to its group slot
+//   bm_score_kernel    persistent, one CTA per SM over a contiguous range of
+//                      groups: a window loader, 3 MMA issuers (which also load
+//                      the query tiles) and 12 epilogue warps (which fetch
+//                      their groups' params)
+//
+// The formula is the indexer's score ("sparse_mqa_indexer" docs, the
+// SparseMQAIndexer forward's MQA-logits call); the record and group layout is
+// in smq_kernels.cuh.
+#include "smq_kernels.cuh"
+#include "smq_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace smq {
+
+namespace {
+
+constexpr uint32_t kAll = 0xffffffffu;
+constexpr uint32_t kTypeE2M1 = 5, kTypeE4M3 = 0;
+constexpr int kBmAcc = 3;                                   // TMEM accumulators of kBmN columns
+constexpr int kBmN = 128;                                   // MMA N: two rows of 64 heads
+constexpr int kBmHeads = 64;
+constexpr int kQRowBytes = kBmHeads * 128;                  // one row's query tile
+constexpr int kRowParamBytes = kBmRowParams * 4;            // 272
+constexpr int kParamBytes = 32 + 2 * kRowParamBytes;        // a group's descriptor and its rows' params
+constexpr int kWindowBytes = 128 * 128;                     // 128 keys in 16-byte containers
+constexpr int kQPer = kBmStages / kBmAcc;                    // query stages of each MMA issuer
+constexpr int kPrmPer = 3;                                  // params slots of each epilogue warpgroup
+constexpr int kBmEpiWarp0 = 1 + kBmAcc;                     // first epilogue warp; warp 0 is the stager
+constexpr int kRecordWarps = 8;
+static_assert(kBmStages % kBmAcc == 0 && kQPer >= 2, "each issuer owns at least two query stages");
+
+struct BmLayout {  // offsets from the 1024-byte aligned base of dynamic shared memory
+  static constexpr uint32_t window = 0;                                   // 2 x 16 KB
+  static constexpr uint32_t q = 2 * kWindowBytes;                         // kBmStages x 16 KB
+  static constexpr uint32_t window_sf = q + kBmStages * 2 * kQRowBytes;   // 2 x 512 B
+  static constexpr uint32_t sf_one = window_sf + 2 * 512;                 // 512 B of 0x7F
+  static constexpr uint32_t prm = sf_one + 512;                           // kBmAcc x kPrmPer x kParamBytes
+  static constexpr uint32_t bars = prm + kBmAcc * kPrmPer * kParamBytes;
+  static constexpr int nbars = 4 + 2 * kBmStages + 3 * kBmAcc;
+  static constexpr uint32_t misc = bars + nbars * 8;                      // TMEM address, abort flag
+  static constexpr uint32_t bytes = misc + 16;
+};
+static_assert(BmLayout::prm % 16 == 0 && kParamBytes % 16 == 0 && kRowParamBytes % 16 == 0,
+              "16-byte aligned params");
+static_assert(BmLayout::bars % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(kBmAcc * kBmN + 12 * kBmAcc <= 512, "accumulators, each issuer's window and query scales fit in TMEM");
+
+__device__ __forceinline__ void status_or(int32_t* s, int code) { atomicOr(s, code); }
+__device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ uint16_t round_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// Two independent fp32 fused multiply-adds, each rounded to nearest even.
+__device__ __forceinline__ void fma2(float2& acc, float wa, float wb, float xa, float xb) {
+  asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%0, %1};\n"
+      " fma.rn.f32x2 c, a, b, c;\n mov.b64 {%0, %1}, c;\n}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "f"(wa), "f"(wb), "f"(xa), "f"(xb));
+}
+
+// Entry j of a row's sparse list: whether it names a sub-block inside the
+// workspace, its window u (relative to the row's ks) and its slot there.
+struct Entry {
+  bool ok;
+  int u;
+  int slot;
+};
+
+__device__ __forceinline__ Entry decode_entry(const int32_t* si, int j, int64_t ks, const BmIndexParams& p, int shift) {
+  Entry e;
+  const int sb = si[j];
+  const int64_t rel = static_cast<int64_t>(sb) << shift;
+  const int64_t pos = ks + rel;
+  e.ok = sb >= 0 && ks >= 0 && pos < p.total_len;
+  e.u = static_cast<int>(rel >> 7);
+  e.slot = static_cast<int>((rel & 127) >> shift);
+  return e;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Index
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kRecordWarps * 32) bm_records_kernel(const __grid_constant__ BmIndexParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kRecordWarps + warp;
+  if (r >= p.rows) return;
+  // the row's epilogue parameters: its 64 head weights as float, then q_scale
+  float* rp = p.rowparams + static_cast<int64_t>(r) * kBmRowParams;
+  const uint32_t w2 = reinterpret_cast<const uint32_t*>(p.weights + static_cast<int64_t>(r) * kBmHeads)[lane];
+  reinterpret_cast<float2*>(rp)[lane] = make_float2(bf16_bits(w2 & 0xffffu), bf16_bits(w2 >> 16));
+  if (lane < 4) rp[kBmHeads + lane] = lane == 0 ? p.q_scale[r] : 0.f;
+
+  int e = p.end[r];
+  e = e < 0 ? 0 : (e > p.num_cols ? p.num_cols : e);
+  const int shift = 31 - __clz(p.sbkv);  // the sub-block size is a power of two
+  const int nent = (e + p.sbkv - 1) >> shift;  // entries holding at least one valid column
+  const int64_t ks = p.row_ks[r];
+  const int32_t* si = p.sparse_indices + static_cast<int64_t>(r) * p.nsb;
+  int nrec = 0;
+  Entry prev{false, 0, 0};  // the entry before this chunk
+  for (int base = 0; base < nent; base += 32) {
+    const int j = base + lane;
+    Entry cur{false, 0, 0};
+    if (j < nent) {
+      cur = decode_entry(si, j, ks, p, shift);
+      if (!cur.ok) status_or(p.status, kStatusBounds);
+    }
+    Entry before;
+    before.ok = __shfl_up_sync(kAll, cur.ok ? 1 : 0, 1) != 0;
+    before.u = __shfl_up_sync(kAll, cur.u, 1);
+    before.slot = __shfl_up_sync(kAll, cur.slot, 1);
+    if (lane == 0) before = prev;
+    // a record starts at every valid entry that does not continue its
+    // predecessor's run (same window, higher slot)
+    const bool head = cur.ok && !(before.ok && before.u == cur.u && before.slot < cur.slot);
+    const uint32_t heads = __ballot_sync(kAll, head);
+    if (head) {
+      uint32_t mask = 1u << cur.slot;
+      int last = cur.slot;
+      for (int t = j + 1; t < nent; ++t) {  // at most 128 / sbkv - 1 steps: the slots rise
+        const Entry nx = decode_entry(si, t, ks, p, shift);
+        if (!nx.ok || nx.u != cur.u || nx.slot <= last) break;
+        mask |= 1u << nx.slot;
+        last = nx.slot;
+      }
+      const int k = nrec + __popc(heads & ((1u << lane) - 1u));
+      const int P = static_cast<int>(ks + (static_cast<int64_t>(cur.u) << 7));
+      p.rec[static_cast<int64_t>(r) * p.nsb + k] = make_int2(P, static_cast<int>((static_cast<uint32_t>(j) << shift) | (mask << 24)));
+      atomicAdd(p.cnt + P, 1);
+    }
+    nrec += __popc(heads);
+    prev.ok = __shfl_sync(kAll, cur.ok ? 1 : 0, 31) != 0;
+    prev.u = __shfl_sync(kAll, cur.u, 31);
+    prev.slot = __shfl_sync(kAll, cur.slot, 31);
+  }
+  if (lane == 0) p.nrec[r] = nrec;
+}
+
+// Groups of two records per window, windows in position order: cursor[P]
+// becomes the first record slot of window P (2 x its first group). Thread t
+// scans a contiguous chunk of positions (a multiple of 4, read 32 at a time
+// with 16-byte loads issued together), then a block scan gives its offset.
+constexpr int kPlanBatch = 32;
+
+__device__ __forceinline__ void load_counts(const int32_t* cnt, int64_t i0, int64_t hi, int (&c)[kPlanBatch]) {
+#pragma unroll
+  for (int k = 0; k < kPlanBatch / 4; ++k) {
+    const int64_t i = i0 + 4 * k;
+    if (i + 4 <= hi) {
+      const int4 v = *reinterpret_cast<const int4*>(cnt + i);
+      c[4 * k] = v.x;
+      c[4 * k + 1] = v.y;
+      c[4 * k + 2] = v.z;
+      c[4 * k + 3] = v.w;
+    } else {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) c[4 * k + x] = i + x < hi ? cnt[i + x] : 0;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) bm_plan_kernel(const __grid_constant__ BmIndexParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t per = ((p.total_len + 1023) / 1024 + 3) & ~int64_t(3);
+  const int64_t lo = min(p.total_len, static_cast<int64_t>(tid) * per);
+  const int64_t hi = min(p.total_len, lo + per);
+  int mine = 0;
+  for (int64_t i0 = lo; i0 < hi; i0 += kPlanBatch) {
+    int c[kPlanBatch];
+    load_counts(p.cnt, i0, hi, c);
+#pragma unroll
+    for (int k = 0; k < kPlanBatch; ++k) mine += (c[k] + 1) >> 1;
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kAll, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = wsum[lane];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, x, o);
+      if (lane >= o) x += y;
+    }
+    wsum[lane] = x - v;
+  }
+  __syncthreads();
+  int g = wsum[warp] + incl - mine;
+  for (int64_t i0 = lo; i0 < hi; i0 += kPlanBatch) {
+    int c[kPlanBatch];
+    load_counts(p.cnt, i0, hi, c);
+#pragma unroll
+    for (int k = 0; k < kPlanBatch; ++k) {
+      if (c[k] == 0) continue;
+      p.cursor[i0 + k] = 2 * g;
+      if (c[k] & 1) p.groups[g + (c[k] >> 1)].row[1] = -1;  // the window's last group holds one record
+      g += (c[k] + 1) >> 1;
+    }
+  }
+  if (tid == 1023) *p.ngroups = g;
+}
+
+__global__ void __launch_bounds__(kRecordWarps * 32) bm_fill_kernel(const __grid_constant__ BmIndexParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kRecordWarps + warp;
+  if (r >= p.rows) return;
+  int e = p.end[r];
+  e = e < 0 ? 0 : (e > p.num_cols ? p.num_cols : e);
+  const int n = p.nrec[r];
+  for (int k = lane; k < n; k += 32) {
+    const int2 rc = p.rec[static_cast<int64_t>(r) * p.nsb + k];
+    const int at = atomicAdd(p.cursor + rc.x, 1);
+    BmGroup* g = p.groups + (at >> 1);
+    const int s = at & 1;
+    if (s == 0) g->P = rc.x;
+    g->row[s] = r;
+    g->c0m[s] = rc.y;
+    g->end[s] = e;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Score
+// ---------------------------------------------------------------------------
+
+// Warps: 0 window loader, 1..3 MMA issuers, 4..15 epilogue (three
+// warpgroups). Issuer t and epilogue warpgroup t own accumulator t and take
+// the groups it = t, t + 3, ...; issuer t also loads the query tiles of its
+// groups into its own kQPer stages, and warpgroup t fetches their params
+// into its own ring. So every barrier has one waiter that sees its phases in
+// order (a parity wait cannot match a phase two back), except the windows',
+// which every issuer waits for in order.
+__global__ void __launch_bounds__(kBmThreads, 1)
+    bm_score_kernel(const __grid_constant__ BmScoreParams p, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_kw) {
+  using L = BmLayout;
+  extern __shared__ uint8_t bm_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bm_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int NS = kBmStages;
+  constexpr int NA = kBmAcc;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+  auto win_full = [&](int i) { return smem_addr(&bars[i]); };
+  auto win_empty = [&](int i) { return smem_addr(&bars[2 + i]); };
+  auto q_full = [&](int s) { return smem_addr(&bars[4 + s]); };
+  auto q_empty = [&](int s) { return smem_addr(&bars[4 + NS + s]); };
+  auto acc_full = [&](int a) { return smem_addr(&bars[4 + 2 * NS + a]); };
+  auto acc_empty = [&](int a) { return smem_addr(&bars[4 + 2 * NS + NA + a]); };
+  auto bar_drain = [&](int a) { return smem_addr(&bars[4 + 2 * NS + 2 * NA + a]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
+  const volatile int never = 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(win_full(i), 1);    // the stager's arrival plus the value copy's bytes
+      mbar_init(win_empty(i), NA);  // a commit of each MMA issuer
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(q_full(s), 1);   // the issuer's expect plus its copies' bytes
+      mbar_init(q_empty(s), 1);  // the issuer's MMA commit
+    }
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 4);  // the warpgroup of accumulator a
+      mbar_init(bar_drain(a), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_kw);
+  }
+  // query scales are all 2^0: one 512-byte block of 0x7F for the SF-B columns
+  uint32_t* sf_one = reinterpret_cast<uint32_t*>(smem + L::sf_one);
+  if (tid < 128) sf_one[tid] = 0x7F7F7F7Fu;
+  fence_proxy_async_smem();
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_sfa = tmem + NA * kBmN;  // per MMA issuer t: 4 columns per window slot at 8 t
+  const uint32_t tm_sfb = tm_sfa + 8 * NA;   // per MMA issuer t: 4 columns at 4 t
+
+  // everything below reads what the index kernels wrote
+  griddep_launch_dependents();
+  griddep_wait();
+  const int G = *p.ngroups;
+  const int g_begin = static_cast<int>(static_cast<int64_t>(G) * blockIdx.x / gridDim.x);
+  const int g_end = static_cast<int>(static_cast<int64_t>(G) * (blockIdx.x + 1) / gridDim.x);
+  const int n = g_end - g_begin;
+  const BmGroup* groups = p.groups + g_begin;
+
+  if (warp == 0) {
+    // ======================= window loader =======================
+    // Walks the groups' window ids in order (batches of 32, one batch ahead).
+    // A new window: its 128 rows of values by one tensor copy that unpacks
+    // E2M1 into the MMA's containers (positions past the workspace read as
+    // zero), its scale words through registers into the layout tcgen05.cp
+    // places at lane m, column m / 32: word 4 (m % 32) + m / 32.
+    bool ok = true;
+    int nw = 0, cur = -1;
+    const uint32_t* scales = reinterpret_cast<const uint32_t*>(p.k_scales);
+    auto load_P = [&](int b) { return b + lane < n ? groups[b + lane].P : -1; };
+    auto walk = [&](int base, int myP) {
+      for (int k = 0; k < 32 && base + k < n && ok; ++k) {
+        const int P = __shfl_sync(kAll, myP, k);
+        if (P == cur) continue;
+        cur = P;
+        const int slot = nw & 1;
+        ok = warp_wait(win_empty(slot), ((nw >> 1) & 1) ^ 1, abort_flag, p.wait_ns);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(win_full(slot), 128 * (kHeadDim / 2));  // the packed source bytes
+          tma_load_3d(smem_addr(smem + L::window + slot * kWindowBytes), &tm_kw, 0, P, 0, win_full(slot));
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t pos = static_cast<int64_t>(P) + 32 * q + lane;
+          w[q] = pos < p.total_len ? __ldg(scales + pos) : 0x7F7F7F7Fu;
+        }
+        const uint32_t sdst = smem_addr(smem + L::window_sf + slot * 512 + 16 * lane);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sdst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(win_full(slot));
+        ++nw;
+      }
+    };
+    int pa = load_P(0);
+    for (int base = 0; base < n && ok; base += 64) {
+      const int pb = load_P(base + 32);
+      walk(base, pa);
+      pa = load_P(base + 64);
+      walk(base + 32, pb);
+    }
+    if (!ok) {
+      if (lane == 0) status_or(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // the last windows' copies may still be in flight when another warp gave up
+    if (lane == 0)
+      for (int t = nw > 2 ? nw - 2 : 0; t < nw; ++t) mbar_wait(win_full(t & 1), (t >> 1) & 1, &never, p.wait_ns);
+    __syncwarp();
+  } else if (warp <= NA) {
+    // ======================= MMA issuers =======================
+    // Issuing tcgen05 instructions costs a thread about as much as they take
+    // to run, so three threads share it. Issuer t follows the window sequence
+    // of all groups (the descriptors come from the group list in global
+    // memory, batches of 32 one batch ahead) and keeps its own scale columns;
+    // a window's slot is free once every issuer committed past it. A window
+    // an issuer has no group in is committed after it has loaded (so that a
+    // commit for the slot's next window cannot pass it). For its own group k
+    // it first loads the query tiles of its group k + kQPer - 1 into stage
+    // (k + kQPer - 1) % kQPer of its own. Lane 0 issues.
+    const int t = warp - 1;
+    const uint32_t sfa = tm_sfa + 8 * t, sfb = tm_sfb + 4 * t;
+    uint32_t idesc[4];
+    for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kTypeE2M1, kTypeE4M3, 128, kBmN, g, g);
+    if (lane == 0) tmem_cp_32x128b_x4(sfb, rows16_desc(smem_addr(sf_one)));
+    bool ok = true;
+    int cur = -1, nw = 0;  // window id and count over the groups scanned so far
+    int mine = -1;         // the window this issuer is in
+    int scan = 0;          // next group to scan for a window change
+    int issued = 0;        // own groups whose query tiles are out
+    int base = 0;
+    auto load4 = [&](int b) {
+      return b + lane < n ? *reinterpret_cast<const int4*>(groups + b + lane) : make_int4(-1, -1, -1, 0);
+    };
+    int4 dcur = load4(0), dnxt = load4(32);  // (P, row0, row1, c0m0) of groups base + lane, base + 32 + lane
+    auto field = [&](int g, int f) {         // field f of group g, base <= g < base + 64 (g uniform)
+      const int d = g - base;
+      const int4 src = d < 32 ? dcur : dnxt;
+      const int v = f == 0 ? src.x : (f == 1 ? src.y : src.z);
+      return __shfl_sync(kAll, v, d & 31);
+    };
+    auto pass_windows = [&](int upto) {  // lane 0: commit windows [max(mine, 0), upto) this issuer leaves
+      for (int w = mine < 0 ? 0 : mine; w < upto && ok; ++w) {
+        if (w != mine) ok = mbar_wait(win_full(w & 1), (w >> 1) & 1, abort_flag, p.wait_ns);
+        mma_commit(win_empty(w & 1));
+      }
+    };
+    auto load_q = [&](int k) {  // query tiles of own group k (k < count of own groups)
+      const int g = t + NA * k;
+      const int r0 = field(g, 1), r1 = field(g, 2);
+      if (lane == 0) {
+        const int s = t * kQPer + k % kQPer;
+        ok = ok && mbar_wait(q_empty(s), ((k / kQPer) & 1) ^ 1, abort_flag, p.wait_ns);
+        if (ok && !(g == p.stall_group && blockIdx.x == 0)) {
+          const uint32_t qdst = smem_addr(smem + L::q + s * 2 * kQRowBytes);
+          mbar_arrive_expect_tx(q_full(s), (r1 >= 0 ? 2 : 1) * kQRowBytes);
+          tma_load_2d(qdst, &tm_q, 0, r0 * kBmHeads, q_full(s));
+          if (r1 >= 0) tma_load_2d(qdst + kQRowBytes, &tm_q, 0, r1 * kBmHeads, q_full(s));
+        }
+      }
+      ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+      issued = k + 1;
+    };
+    const int own = n > t ? (n - t + NA - 1) / NA : 0;  // own groups
+    for (int k = 0; k < kQPer - 1 && k < own && ok; ++k) load_q(k);
+    for (int k = 0; k < own && ok; ++k) {
+      const int it = t + NA * k;
+      for (; scan <= it; ++scan) {  // window changes of every group up to this one
+        const int P = field(scan, 0);
+        if (P != cur) {
+          cur = P;
+          ++nw;
+        }
+      }
+      if (it >= base + 32) {  // slide the descriptor batches: the next one was loaded a batch ago
+        base += 32;
+        dcur = dnxt;
+        dnxt = load4(base + 32);
+      }
+      if (k + kQPer - 1 < own) load_q(k + kQPer - 1);
+      if (!ok) break;
+      if (lane == 0) {
+        const int wi = nw - 1;
+        if (wi != mine) {
+          pass_windows(wi);
+          ok = ok && mbar_wait(win_full(wi & 1), (wi >> 1) & 1, abort_flag, p.wait_ns);
+          if (ok) {
+            tc_fence_after();
+            tmem_cp_32x128b_x4(sfa + 4 * (wi & 1), rows16_desc(smem_addr(smem + L::window_sf + (wi & 1) * 512)));
+            mine = wi;
+          }
+        }
+        const int s = t * kQPer + k % kQPer;
+        ok = ok && mbar_wait(q_full(s), (k / kQPer) & 1, abort_flag, p.wait_ns) &&
+             mbar_wait(acc_empty(t), (k & 1) ^ 1, abort_flag, p.wait_ns);
+        if (ok) {
+          tc_fence_after();
+          const int slot = wi & 1;
+          const uint64_t adesc = sw128_desc(smem_addr(smem + L::window + slot * kWindowBytes));
+          const uint64_t bdesc = sw128_desc(smem_addr(smem + L::q + s * 2 * kQRowBytes));
+#pragma unroll
+          for (int g = 0; g < 4; ++g)  // K = 32 per MMA: 32 bytes along the swizzled rows
+            mma_mxf8f6f4(tmem + t * kBmN, adesc + 2 * g, bdesc + 2 * g, idesc[g], sfa + 4 * slot, sfb, g > 0);
+          mma_commit(acc_full(t));
+          mma_commit(q_empty(s));
+        }
+      }
+      ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
+      if (ok) {  // the windows left: this issuer's last and those with none of its groups
+        for (; scan < n; ++scan) {
+          // the remaining groups' window ids, read directly (lane 0 alone)
+          const int P = groups[scan].P;
+          if (P != cur) {
+            cur = P;
+            ++nw;
+          }
+        }
+        pass_windows(nw);
+      }
+      if (!ok) {
+        status_or(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        // query tiles issued but not consumed may still be in flight: let them land
+        for (int k = issued > kQPer ? issued - kQPer : 0; k < issued; ++k)
+          mbar_wait(q_full(t * kQPer + k % kQPer), (k / kQPer) & 1, &never, p.wait_ns);
+      }
+      mma_commit(bar_drain(t));  // every tcgen05 operation of this thread has finished once this arrives
+      mbar_wait(bar_drain(t), 0, &never, p.wait_ns);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue (warps 4..15) =======================
+    // Warpgroup t takes the groups it = t, t + 3, ... whole (both rows), so
+    // that the warps sharing a scheduler are at different points of different
+    // groups. It fetches each group's descriptor and its rows' params itself,
+    // one group ahead, by 16-byte asynchronous copies (one per thread) into a
+    // ring of kPrmPer slots of its own; the rows of the group after that come
+    // from a load two groups ahead. A named barrier per warpgroup publishes
+    // the copies and frees the slots.
+    const int wg = (warp - kBmEpiWarp0) >> 2;
+    const int wt = tid - 32 * (kBmEpiWarp0 + 4 * wg);  // thread of the warpgroup
+    const int q4 = warp & 3;        // TMEM lane quarter
+    const int m = 32 * q4 + lane;   // key of the window
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const int shift = 31 - __clz(p.sbkv);
+    const int sl = m >> shift;
+    const uint32_t below = (1u << sl) - 1u;
+    const int moff = m & (p.sbkv - 1);
+    const int own = n > wg ? (n - wg + NA - 1) / NA : 0;
+    constexpr int kChunks = (kParamBytes + 15) / 16;  // 36: descriptor, then the two rows' params
+    static_assert(kChunks <= 128, "one chunk per thread of the warpgroup");
+    auto fetch = [&](int k, int r0, int r1) {  // group k's descriptor and params into slot k % kPrmPer
+      if (k < own && wt < kChunks) {
+        const uint32_t dst = smem_addr(smem + L::prm + (wg * kPrmPer + k % kPrmPer) * kParamBytes) + 16 * wt;
+        const uint8_t* src;
+        if (wt < 2) {
+          src = reinterpret_cast<const uint8_t*>(groups + wg + NA * k) + 16 * wt;
+        } else {
+          const int c = wt - 2, e = c / (kRowParamBytes / 16), off = c % (kRowParamBytes / 16);
+          const int r = e == 0 ? r0 : r1;
+          src = reinterpret_cast<const uint8_t*>(p.rowparams + static_cast<int64_t>(r < 0 ? r0 : r) * kBmRowParams) + 16 * off;
+        }
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto rows_of = [&](int k) {  // (row0, row1) of group k, or (-1, -1)
+      if (k >= own) return make_int2(-1, -1);
+      const int4 d = *reinterpret_cast<const int4*>(groups + wg + NA * k);
+      return make_int2(d.y, d.z);
+    };
+    int2 r1n = rows_of(1);  // rows of the next group
+    {
+      const int2 r0n = rows_of(0);
+      fetch(0, r0n.x, r0n.y);
+    }
+    bool ok = true;
+    for (int k = 0; k < own && ok; ++k) {
+      const int2 r2n = rows_of(k + 2);  // used next step
+      fetch(k + 1, r1n.x, r1n.y);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's copies of group k
+      const int a = wg;
+      ok = warp_wait(acc_full(a), k & 1, abort_flag, p.wait_ns);
+      // every thread's copies of group k are in, slot k - 1 is read; and the
+      // warpgroup agrees on going on (a wait that gave up stops all four warps)
+      uint32_t all_ok;
+      asm volatile(
+          "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, %2, 128, pi;\n"
+          " selp.u32 %0, 1, 0, po;\n}"
+          : "=r"(all_ok)
+          : "r"(ok ? 1u : 0u), "r"(1 + wg)
+          : "memory");
+      ok = all_ok != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint8_t* prm = smem + L::prm + (wg * kPrmPer + k % kPrmPer) * kParamBytes;
+      const BmGroup* gd = reinterpret_cast<const BmGroup*>(prm);
+#pragma unroll 1
+      for (int e = 0; e < 2; ++e) {
+        const int row = gd->row[e];
+        uint32_t v[64];
+        const uint32_t tacc = tmem + a * kBmN + e * kBmHeads + lane_base;
+        tmem_ld16(tacc, *reinterpret_cast<uint32_t(*)[16]>(v));
+        tmem_ld16(tacc + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        tmem_ld16(tacc + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
+        tmem_ld16(tacc + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
+        tmem_wait_ld();
+        if (e == 1) {  // every column of the accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(a));
+        }
+        if (row < 0) continue;
+        const float4* w4 = reinterpret_cast<const float4*>(prm + 32 + e * kRowParamBytes);
+        // heads h = 0, 1 (mod 4) in lo, h = 2, 3 (mod 4) in hi, each in head order
+        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 w = w4[h4];
+          fma2(lo, w.x, w.y, fmaxf(__uint_as_float(v[4 * h4]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f));
+          fma2(hi, w.z, w.w, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f));
+        }
+        const float qs = reinterpret_cast<const float*>(prm + 32 + e * kRowParamBytes)[kBmHeads];
+        const float logit = ((lo.x + lo.y) + (hi.x + hi.y)) * qs;
+        const uint32_t c0m = static_cast<uint32_t>(gd->c0m[e]);
+        const uint32_t mask = c0m >> 24;
+        if ((mask >> sl) & 1u) {
+          const int col = static_cast<int>(c0m & 0xFFFFFFu) + (__popc(mask & below) << shift) + moff;
+          if (col < gd->end[e]) {
+            const int64_t at = static_cast<int64_t>(row) * p.num_cols + col;
+            p.logits[at] = logit;
+            if (p.logits_bf16) p.logits_bf16[at] = round_bf16(logit);
+          }
+        }
+      }
+      r1n = r2n;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy into shared memory outlives the CTA
+    if (!ok) {
+      if (lane == 0) status_or(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+
+namespace {
+
+template <typename... A>
+cudaError_t launch_pdl_bm(void (*kernel)(A...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                          const A&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+
+size_t bm_score_smem_bytes() { return BmLayout::bytes + 1024; }
+
+cudaError_t prepare_bm_kernels() {
+  cudaError_t err = cudaFuncSetAttribute(bm_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bm_score_smem_bytes()));
+  if (err != cudaSuccess) return err;
+  const void* all[] = {reinterpret_cast<const void*>(&bm_score_kernel),
+                       reinterpret_cast<const void*>(&bm_records_kernel),
+                       reinterpret_cast<const void*>(&bm_plan_kernel), reinterpret_cast<const void*>(&bm_fill_kernel)};
+  for (const void* f : all) {
+    err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_bm_index(const BmIndexParams& p, cudaStream_t stream) {
+  cudaError_t err = cudaMemsetAsync(p.cnt, 0, static_cast<size_t>(p.total_len) * sizeof(int32_t), stream);
+  if (err != cudaSuccess) return err;
+  const unsigned row_grid = static_cast<unsigned>((p.rows + kRecordWarps - 1) / kRecordWarps);
+  err = launch_pdl_bm(bm_records_kernel, row_grid, kRecordWarps * 32, 0, stream, p);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl_bm(bm_plan_kernel, 1, 1024, 0, stream, p);
+  if (err != cudaSuccess) return err;
+  return launch_pdl_bm(bm_fill_kernel, row_grid, kRecordWarps * 32, 0, stream, p);
+}
+
+cudaError_t launch_bm_score(const BmScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kw, int grid,
+                            cudaStream_t stream) {
+  return launch_pdl_bm(bm_score_kernel, static_cast<unsigned>(grid), kBmThreads, bm_score_smem_bytes(), stream, p, tm_q,
+                       tm_kw);
+}
+
+}  // namespace smq

@@ -69,10 +69,11 @@ class DecodeDevice:
 
 
 class PrefillDevice:
-    """Device copies of a PrefillInputs (paged cache + gathered workspace) plus outputs."""
+    """Device copies of a PrefillInputs (paged cache + gathered workspace) plus outputs. With window_major the
+    workspace also holds the window-major path's scratch (the call then takes that path)."""
 
     def __init__(self, inp, plan: Plan, with_logits: bool = True, with_cols: bool = True,
-                 with_logits_bf16: bool = False):
+                 with_logits_bf16: bool = False, window_major: bool = True):
         dev = plan.device
         R = inp.rows
         self.rows = R
@@ -96,7 +97,8 @@ class PrefillDevice:
                                  device=dev) if with_logits else None
         self.logits_bf16 = torch.full((R, plan.num_sparse_cols), 0x7FC1, dtype=torch.int16,
                                       device=dev) if with_logits_bf16 else None
-        self.workspace = plan.workspace(max(R, 1))
+        # sized for the window-major prefill path, or for the row-major one only
+        self.workspace = plan.workspace(max(R, 1), total_len=self.total_len if window_major else None)
 
     def gather(self, plan: Plan, stream=None) -> None:
         sparse_mqa_gather_k(plan, self.k_cache, self.seq_block_table, self.cu_seq_lens, self.total_len,

@@ -65,9 +65,12 @@ def test_timeout_in_the_persistent_kernel():
 def test_timeout_in_the_tensor_copy_paths():
     pf = synth.prefill_chunk(seed=95, seq_lens=(1500, 2300), queries_per_seq=90, num_heads=64, page_size=64,
                              cbs=128, ncb=8, topk=200)
-    plan, dev = _stall_then_recover(pf, _prefill, tensors.PrefillDevice)  # contiguous workspace
     kv, ks = oracle.gather_reference(pf)
-    check_rows(pf, dev, plan, oracle.reference_rows(pf, rows=range(0, pf.rows, 13), mode="sparse", contig=(kv, ks)))
+    for window_major in (True, False):  # the window-major kernel; the row-major one on the contiguous workspace
+        plan, dev = _stall_then_recover(pf, _prefill,
+                                        lambda i, p, wm=window_major: tensors.PrefillDevice(i, p, window_major=wm))
+        check_rows(pf, dev, plan,
+                   oracle.reference_rows(pf, rows=range(0, pf.rows, 13), mode="sparse", contig=(kv, ks)))
     dec = synth.prefill_as_decode(pf)  # 180 rows on 2 block-table rows: paged tensor copies
     plan, dev = _stall_then_recover(dec, _decode, tensors.DecodeDevice)
     check_rows(dec, dev, plan, oracle.reference_rows(dec, rows=range(0, dec.rows, 13), mode="sparse"))

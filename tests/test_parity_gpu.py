@@ -167,6 +167,31 @@ def test_prefill_unaligned_sequence_starts():
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
 
 
+@pytest.mark.parametrize("seq_lens,page,cbs,ncb,seed", [
+    ((1021, 999, 1502), 32, 64, 9, 31),    # 4 slots per window, two per block; unaligned starts
+    ((2000, 1777), 64, 256, 5, 32),        # a block spans two windows
+    ((900, 1300, 517), 16, 16, 40, 33),    # 8 slots per window, one per block
+])
+def test_window_major_prefill_matches_the_row_major_path(seq_lens, page, cbs, ncb, seed):
+    """The window-major prefill (rows grouped by the 128-key windows they
+    selected, two rows per MMA) gives the row-major kernel's logits and ids
+    bit for bit, and both match the oracle; windows hold partial slot masks,
+    sequence starts are not multiples of 128 and windows run past the end of
+    the workspace."""
+    inp = synth.prefill_chunk(seed=seed, seq_lens=seq_lens, queries_per_seq=30, num_heads=64, page_size=page,
+                              cbs=cbs, ncb=ncb, topk=150)
+    plan, wm, status = run_prefill(inp, window_major=True)
+    _ok(status)
+    _, rm, status = run_prefill(inp, plan=plan, window_major=False)
+    _ok(status)
+    assert torch.equal(wm.sparse_indices, rm.sparse_indices) and torch.equal(wm.end, rm.end)
+    valid = torch.arange(plan.num_sparse_cols, device=wm.end.device)[None, :] < wm.end[:, None].long()
+    assert torch.equal(wm.logits[valid], rm.logits[valid])
+    assert torch.equal(wm.topk_out, rm.topk_out)
+    kv, ks = oracle.gather_reference(inp)
+    check_rows(inp, wm, plan, oracle.reference_rows(inp, mode="dense", contig=(kv, ks)))
+
+
 def test_prefill_rows_through_the_paged_decode_call():
     """In-place paged prefill: the chunk's rows, run through the paged decode
     call on the cache itself, give the gather path's expansion, logits and ids."""
