@@ -286,6 +286,7 @@ struct BmIndexParams {
   float* rowparams;               // [rows][kBmRowParams]
   BmGroup* groups;                // [rows * nsb]
   int32_t* ngroups;               // [1]
+  int32_t* tile_groups;           // [ceil(total_len / 2048)] groups per tile of positions
   int32_t* status;
 };
 
@@ -305,7 +306,7 @@ struct BmScoreParams {
 };
 
 size_t bm_score_smem_bytes();
-cudaError_t launch_bm_index(const BmIndexParams& p, cudaStream_t stream);  // zeroes cnt, then 3 kernels
+cudaError_t launch_bm_index(const BmIndexParams& p, cudaStream_t stream);  // zeroes cnt, then 4 kernels
 cudaError_t launch_bm_score(const BmScoreParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kw, int grid,
                             cudaStream_t stream);
 cudaError_t prepare_bm_kernels();

@@ -12,8 +12,9 @@
 //
 //   bm_records_kernel  one warp per row: the row's (row, window) records, the
 //                      per-window record counts, the row's float weights
-//   bm_plan_kernel     one CTA: groups of two records per window, numbered
-//                      window by window (an exclusive scan over positions)
+//   bm_tilesum_kernel  groups of two records per window, summed per tile of
+//   bm_plan_kernel     positions; then numbered window by window (each tile
+//                      offset by the tiles before it, scanned within)
 //   bm_fill_kernel     one warp per row: each record to its group slot
 //   bm_score_kernel    persistent, one CTA per SM over a contiguous range of
 //                      groups: a window loader, 3 MMA issuers (which also load
@@ -159,75 +160,98 @@ __global__ void __launch_bounds__(kRecordWarps * 32) bm_records_kernel(const __g
 }
 
 // Groups of two records per window, windows in position order: cursor[P]
-// becomes the first record slot of window P (2 x its first group). Thread t
-// scans a contiguous chunk of positions (a multiple of 4, read 32 at a time
-// with 16-byte loads issued together), then a block scan gives its offset.
-constexpr int kPlanBatch = 32;
+// becomes the first record slot of window P (2 x its first group). Positions
+// go in tiles of kScanTile: one kernel sums each tile's groups, the next gives
+// each tile its offset (the sum of the tiles before it) and scans the tile.
+// Thread t of a tile takes its positions 8 t .. 8 t + 7 (two 16-byte loads).
+constexpr int kScanThreads = 256;
+constexpr int kScanTile = 8 * kScanThreads;
 
-__device__ __forceinline__ void load_counts(const int32_t* cnt, int64_t i0, int64_t hi, int (&c)[kPlanBatch]) {
+__device__ __forceinline__ void load_tile_counts(const int32_t* cnt, int64_t total, int64_t i0, int (&c)[8]) {
+  if (i0 + 8 <= total) {
+    const int4 a = *reinterpret_cast<const int4*>(cnt + i0);
+    const int4 b = *reinterpret_cast<const int4*>(cnt + i0 + 4);
+    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+  } else {
 #pragma unroll
-  for (int k = 0; k < kPlanBatch / 4; ++k) {
-    const int64_t i = i0 + 4 * k;
-    if (i + 4 <= hi) {
-      const int4 v = *reinterpret_cast<const int4*>(cnt + i);
-      c[4 * k] = v.x;
-      c[4 * k + 1] = v.y;
-      c[4 * k + 2] = v.z;
-      c[4 * k + 3] = v.w;
-    } else {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) c[4 * k + x] = i + x < hi ? cnt[i + x] : 0;
-    }
+    for (int x = 0; x < 8; ++x) c[x] = i0 + x < total ? cnt[i0 + x] : 0;
   }
 }
 
-__global__ void __launch_bounds__(1024) bm_plan_kernel(const __grid_constant__ BmIndexParams p) {
-  griddep_launch_dependents();
-  griddep_wait();
-  __shared__ int wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t per = ((p.total_len + 1023) / 1024 + 3) & ~int64_t(3);
-  const int64_t lo = min(p.total_len, static_cast<int64_t>(tid) * per);
-  const int64_t hi = min(p.total_len, lo + per);
-  int mine = 0;
-  for (int64_t i0 = lo; i0 < hi; i0 += kPlanBatch) {
-    int c[kPlanBatch];
-    load_counts(p.cnt, i0, hi, c);
-#pragma unroll
-    for (int k = 0; k < kPlanBatch; ++k) mine += (c[k] + 1) >> 1;
-  }
-  int incl = mine;
+// Block-wide exclusive scan of one value per thread; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(kAll, incl, o);
-    if (lane >= o) incl += v;
+    const int y = __shfl_up_sync(kAll, incl, o);
+    if (lane >= o) incl += y;
   }
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int v = wsum[lane];
-    int x = v;
+    const int w = lane < kScanThreads / 32 ? wsum[lane] : 0;
+    int x = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(kAll, x, o);
       if (lane >= o) x += y;
     }
-    wsum[lane] = x - v;
+    if (lane < kScanThreads / 32) wsum[lane] = x - w;
+    if (lane == kScanThreads / 32 - 1) wsum[32] = x;
   }
   __syncthreads();
-  int g = wsum[warp] + incl - mine;
-  for (int64_t i0 = lo; i0 < hi; i0 += kPlanBatch) {
-    int c[kPlanBatch];
-    load_counts(p.cnt, i0, hi, c);
+  *total = wsum[32];
+  return wsum[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) bm_tilesum_kernel(const __grid_constant__ BmIndexParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ int wsum[33];
+  int c[8];
+  load_tile_counts(p.cnt, p.total_len, static_cast<int64_t>(blockIdx.x) * kScanTile + 8 * threadIdx.x, c);
+  int mine = 0;
 #pragma unroll
-    for (int k = 0; k < kPlanBatch; ++k) {
-      if (c[k] == 0) continue;
-      p.cursor[i0 + k] = 2 * g;
-      if (c[k] & 1) p.groups[g + (c[k] >> 1)].row[1] = -1;  // the window's last group holds one record
-      g += (c[k] + 1) >> 1;
-    }
+  for (int x = 0; x < 8; ++x) mine += (c[x] + 1) >> 1;
+  int total;
+  block_exclusive_scan(mine, wsum, &total);
+  if (threadIdx.x == 0) p.tile_groups[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kScanThreads) bm_plan_kernel(const __grid_constant__ BmIndexParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ int wsum[33];
+  __shared__ int red[kScanThreads / 32];
+  const int b = blockIdx.x;
+  // this tile's offset: the groups of the tiles before it
+  int before = 0;
+  for (int i = threadIdx.x; i < b; i += kScanThreads) before += p.tile_groups[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(kAll, before, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = before;
+  int c[8];
+  const int64_t i0 = static_cast<int64_t>(b) * kScanTile + 8 * threadIdx.x;
+  load_tile_counts(p.cnt, p.total_len, i0, c);
+  int mine = 0;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) mine += (c[x] + 1) >> 1;
+  int total;
+  int g = block_exclusive_scan(mine, wsum, &total);  // its __syncthreads also publish red[]
+  int offset = 0;
+#pragma unroll
+  for (int w = 0; w < kScanThreads / 32; ++w) offset += red[w];
+  g += offset;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    if (c[x] == 0) continue;
+    p.cursor[i0 + x] = 2 * g;
+    if (c[x] & 1) p.groups[g + (c[x] >> 1)].row[1] = -1;  // the window's last group holds one record
+    g += (c[x] + 1) >> 1;
   }
-  if (tid == 1023) *p.ngroups = g;
+  if (b == gridDim.x - 1 && threadIdx.x == 0) *p.ngroups = offset + total;
 }
 
 __global__ void __launch_bounds__(kRecordWarps * 32) bm_fill_kernel(const __grid_constant__ BmIndexParams p) {
@@ -566,33 +590,46 @@ __global__ void __launch_bounds__(kBmThreads, 1)
       tc_fence_after();
       const uint8_t* prm = smem + L::prm + (wg * kPrmPer + k % kPrmPer) * kParamBytes;
       const BmGroup* gd = reinterpret_cast<const BmGroup*>(prm);
+      const int row0 = gd->row[0], row1 = gd->row[1];
+      // Both rows in two halves of 32 heads: the second half's loads are the
+      // last reads of the accumulator, so it goes back before half of the
+      // arithmetic. Per row, heads h = 0, 1 (mod 4) accumulate in lo and
+      // h = 2, 3 (mod 4) in hi, each in head order.
+      float2 lo[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float2 hi[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 1
-      for (int e = 0; e < 2; ++e) {
-        const int row = gd->row[e];
-        uint32_t v[64];
-        const uint32_t tacc = tmem + a * kBmN + e * kBmHeads + lane_base;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[64];  // row 0 heads 32 half .. + 31, then row 1's
+        const uint32_t tacc = tmem + a * kBmN + 32 * half + lane_base;
         tmem_ld16(tacc, *reinterpret_cast<uint32_t(*)[16]>(v));
         tmem_ld16(tacc + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-        tmem_ld16(tacc + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
-        tmem_ld16(tacc + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
+        tmem_ld16(tacc + kBmHeads, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
+        tmem_ld16(tacc + kBmHeads + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
         tmem_wait_ld();
-        if (e == 1) {  // every column of the accumulator is in registers: hand it back
+        if (half == 1) {  // every column of the accumulator is in registers: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty(a));
         }
-        if (row < 0) continue;
-        const float4* w4 = reinterpret_cast<const float4*>(prm + 32 + e * kRowParamBytes);
-        // heads h = 0, 1 (mod 4) in lo, h = 2, 3 (mod 4) in hi, each in head order
-        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 w = w4[h4];
-          fma2(lo, w.x, w.y, fmaxf(__uint_as_float(v[4 * h4]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f));
-          fma2(hi, w.z, w.w, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f));
+        for (int e = 0; e < 2; ++e) {
+          if (e == 1 && row1 < 0) break;
+          const float4* w4 = reinterpret_cast<const float4*>(prm + 32 + e * kRowParamBytes) + 8 * half;
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 w = w4[h4];
+            const uint32_t* x = v + 32 * e + 4 * h4;
+            fma2(lo[e], w.x, w.y, fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
+            fma2(hi[e], w.z, w.w, fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
+          }
         }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = e == 0 ? row0 : row1;
+        if (row < 0) continue;
         const float qs = reinterpret_cast<const float*>(prm + 32 + e * kRowParamBytes)[kBmHeads];
-        const float logit = ((lo.x + lo.y) + (hi.x + hi.y)) * qs;
+        const float logit = ((lo[e].x + lo[e].y) + (hi[e].x + hi[e].y)) * qs;
         const uint32_t c0m = static_cast<uint32_t>(gd->c0m[e]);
         const uint32_t mask = c0m >> 24;
         if ((mask >> sl) & 1u) {
@@ -653,7 +690,8 @@ cudaError_t prepare_bm_kernels() {
   if (err != cudaSuccess) return err;
   const void* all[] = {reinterpret_cast<const void*>(&bm_score_kernel),
                        reinterpret_cast<const void*>(&bm_records_kernel),
-                       reinterpret_cast<const void*>(&bm_plan_kernel), reinterpret_cast<const void*>(&bm_fill_kernel)};
+                       reinterpret_cast<const void*>(&bm_tilesum_kernel), reinterpret_cast<const void*>(&bm_plan_kernel),
+                       reinterpret_cast<const void*>(&bm_fill_kernel)};
   for (const void* f : all) {
     err = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
@@ -667,7 +705,10 @@ cudaError_t launch_bm_index(const BmIndexParams& p, cudaStream_t stream) {
   const unsigned row_grid = static_cast<unsigned>((p.rows + kRecordWarps - 1) / kRecordWarps);
   err = launch_pdl_bm(bm_records_kernel, row_grid, kRecordWarps * 32, 0, stream, p);
   if (err != cudaSuccess) return err;
-  err = launch_pdl_bm(bm_plan_kernel, 1, 1024, 0, stream, p);
+  const unsigned tiles = static_cast<unsigned>((p.total_len + kScanTile - 1) / kScanTile);
+  err = launch_pdl_bm(bm_tilesum_kernel, tiles, kScanThreads, 0, stream, p);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl_bm(bm_plan_kernel, tiles, kScanThreads, 0, stream, p);
   if (err != cudaSuccess) return err;
   return launch_pdl_bm(bm_fill_kernel, row_grid, kRecordWarps * 32, 0, stream, p);
 }

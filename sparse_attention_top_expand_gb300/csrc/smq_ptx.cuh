@@ -95,42 +95,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
-// The same bounded wait, suspending in the barrier instead of polling: each
-// try_wait sleeps until the phase completes or about `kSuspendNs` pass, so a
-// waiting warp takes no issue slots from the warps doing the work.
-constexpr uint32_t kSuspendNs = 20000;
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.b32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_sleep_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
-                                                uint64_t limit_ns) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ bool warp_sleep_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
-                                                uint64_t limit_ns) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_sleep_wait(bar, parity, abort, limit_ns);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
-}
-
 // The same wait for a whole warp: lane 0 polls, the warp then resumes together
 // (__syncwarp orders the other lanes after lane 0's acquire).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
