@@ -181,12 +181,15 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("smq_kernels.cu", "smq_prefill.cu", "smq_ptx.cuh", "smq_kernels.cuh")
+
+
 def kernel_source_hash() -> str:
     """Hash of the kernel sources with comments and blank space removed, so
     that a comment edit does not orphan the DRAM counters taken on the code."""
     import re
     h = hashlib.sha256()
-    for name in ("smq_kernels.cu", "smq_ptx.cuh", "smq_kernels.cuh"):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "sparse_attention_top_expand_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -262,7 +265,9 @@ def launches_per_step(workload: str, plan, rows: int, layers: int) -> int:
     """Kernel launches of the library in one step of a workload."""
     ncb = plan.candidate_topk_blocks
     if workload == "prefill_chunk":
-        return 4  # gather, expansion, score, top-k
+        # gather, expansion, the window-major index (records, tile sums, plan, fill), score, top-k
+        # (plus a memset of the window counts, not a kernel of the library)
+        return 8
     # paged decode: one cluster per row (one launch, +1 expansion kernel past 64 blocks) for
     # no more rows than SMs, else the persistent score kernel (expansion inside up to 64
     # blocks) and the top-k kernel
@@ -445,11 +450,13 @@ def measure(workload, args, rank, world, dist, device, steps, warmup, headline):
             achieved = flops / t / 1e12
             bf16 = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
             peak = 2.0 * bf16
+            # the gathered chunk takes the window-major kernel; the in-place chunk the persistent one
+            kname = "bm_score_kernel" if prefill else "score_kernel"
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": load_traffic(workload, "score_kernel"),
+                    "frac": achieved / peak, "traffic": load_traffic(workload, kname),
                     "peak_source": f"{peak_src}: 2 x sustained bf16 (fp8 x fp4 block-scaled runs at the fp8 rate)",
                     "frac_of_fp4_rate": achieved / (6.0 * bf16),
-                    "algorithmic_flops_per_launch": flops, "kernel": "score_kernel"}
+                    "algorithmic_flops_per_launch": flops, "kernel": kname}
         else:
             nsub = sum(int(x) for x in (reps[0][0].end.cpu().numpy() + plan.sparse_block_kv - 1)
                        // plan.sparse_block_kv)

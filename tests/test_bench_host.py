@@ -12,7 +12,7 @@ def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     csrc = tmp_path / "sparse_attention_top_expand_gb300" / "csrc"
     csrc.mkdir(parents=True)
     src = os.path.join(bench.ROOT, "sparse_attention_top_expand_gb300", "csrc")
-    for name in ("smq_kernels.cu", "smq_ptx.cuh", "smq_kernels.cuh"):
+    for name in bench.KERNEL_SOURCES:
         shutil.copy(os.path.join(src, name), csrc / name)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     base = bench.kernel_source_hash()
