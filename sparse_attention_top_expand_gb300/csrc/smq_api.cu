@@ -251,10 +251,10 @@ int row_cluster_size(const smq_plan* p, int rows) {
 
 // Window-major prefill scratch, after the common part of the workspace:
 // per-position window counts and cursors, then per-row record counts, the
-// group count, groups per tile of 2048 positions, the (row, window) records,
+// group count, groups and windows per tile of 2048 positions, the (row, window) records,
 // the rows' float params and the groups (at most one per record).
 struct BmScratch {
-  size_t cnt, cursor, nrec, ngroups, tile_groups, rec, rowparams, groups, end;
+  size_t cnt, cursor, nrec, ngroups, tile_groups, tile_windows, rec, rowparams, groups, end;
 };
 
 BmScratch bm_scratch(const smq_plan* p, int64_t rows, int64_t total_len) {
@@ -266,7 +266,8 @@ BmScratch bm_scratch(const smq_plan* p, int64_t rows, int64_t total_len) {
   w.nrec = w.cursor + up(static_cast<size_t>(total_len) * 4);
   w.ngroups = w.nrec + up(static_cast<size_t>(rows) * 4);
   w.tile_groups = w.ngroups + 256;
-  w.rec = w.tile_groups + up(static_cast<size_t>((total_len + 2047) / 2048) * 4);
+  w.tile_windows = w.tile_groups + up(static_cast<size_t>((total_len + 2047) / 2048) * 4);
+  w.rec = w.tile_windows + up(static_cast<size_t>((total_len + 2047) / 2048) * 4);
   w.rowparams = w.rec + up(records * 8);
   w.groups = w.rowparams + up(static_cast<size_t>(rows) * smq::kBmRowParams * 4);
   w.end = w.groups + up(records * sizeof(smq::BmGroup));
@@ -621,6 +622,7 @@ SMQ_API int sparse_mqa_logits_topk_prefill_chunk(const smq_plan* plan, const smq
     ip.groups = reinterpret_cast<smq::BmGroup*>(ws + w.groups);
     ip.ngroups = reinterpret_cast<int32_t*>(ws + w.ngroups);
     ip.tile_groups = reinterpret_cast<int32_t*>(ws + w.tile_groups);
+    ip.tile_windows = reinterpret_cast<int32_t*>(ws + w.tile_windows);
     ip.status = sp.status;
     if (smq::launch_bm_index(ip, s) != cudaSuccess) return SMQ_ERR_CUDA;
     record(a.profile_events[1], s);

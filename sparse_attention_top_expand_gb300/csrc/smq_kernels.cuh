@@ -254,7 +254,7 @@ cudaError_t prepare_kernels(int n_mma);  // raise the dynamic-smem limits once p
 // c0 + popc(mask & ((1 << s) - 1)) * sbkv + m % sbkv.
 // A group is two records of the same window (row[1] = -1 when the window's
 // record count is odd); groups are numbered window by window.
-constexpr int kBmThreads = 512;           // stager, 3 MMA issuers, 3 x 4 epilogue warps
+constexpr int kBmThreads = 896;           // window loader, 3 MMA issuers, 6 x 4 epilogue warps
 constexpr int kBmStages = 9;              // query stages of two rows (16 KB each), 3 per MMA issuer
 constexpr int kBmRowParams = 68;          // floats per row: 64 head weights, q_scale, 3 pad
 constexpr int64_t kBmMaxTotalLen = 1 << 20;  // windows are counted per workspace position
@@ -262,9 +262,9 @@ constexpr int64_t kBmMaxTotalLen = 1 << 20;  // windows are counted per workspac
 struct BmGroup {
   int32_t P;        // first workspace position of the window
   int32_t row[2];   // row of each column half; row[1] = -1 for a lone record
+  int32_t wo;       // window ordinal: the nonempty windows at lower positions
   int32_t c0m[2];   // column of the record's first entry | slot mask << 24
   int32_t end[2];   // the row's valid column count
-  int32_t pad;
 };
 static_assert(sizeof(BmGroup) == 32, "one group descriptor is 32 bytes (a bulk copy unit)");
 
@@ -287,6 +287,7 @@ struct BmIndexParams {
   BmGroup* groups;                // [rows * nsb]
   int32_t* ngroups;               // [1]
   int32_t* tile_groups;           // [ceil(total_len / 2048)] groups per tile of positions
+  int32_t* tile_windows;          // [ceil(total_len / 2048)] nonempty windows per tile
   int32_t* status;
 };
 

@@ -18,8 +18,8 @@
 //   bm_fill_kernel     one warp per row: each record to its group slot
 //   bm_score_kernel    persistent, one CTA per SM over a contiguous range of
 //                      groups: a window loader, 3 MMA issuers (which also load
-//                      the query tiles) and 12 epilogue warps (which fetch
-//                      their groups' params)
+//                      the query tiles) and 24 epilogue warps (which fetch
+//                      their rows' params)
 //
 // The formula is the indexer's score ("sparse_mqa_indexer" docs, the
 // SparseMQAIndexer forward's MQA-logits call); the record and group layout is
@@ -40,10 +40,11 @@ constexpr int kBmN = 128;                                   // MMA N: two rows o
 constexpr int kBmHeads = 64;
 constexpr int kQRowBytes = kBmHeads * 128;                  // one row's query tile
 constexpr int kRowParamBytes = kBmRowParams * 4;            // 272
-constexpr int kParamBytes = 32 + 2 * kRowParamBytes;        // a group's descriptor and its rows' params
 constexpr int kWindowBytes = 128 * 128;                     // 128 keys in 16-byte containers
 constexpr int kQPer = kBmStages / kBmAcc;                    // query stages of each MMA issuer
-constexpr int kPrmPer = 3;                                  // params slots of each epilogue warpgroup
+constexpr int kPrmPer = 3;                                  // params slots of each epilogue warp
+constexpr int kEpiWarps = 8 * kBmAcc;                        // two warpgroups per accumulator, one per row
+constexpr int kSlotBytes = 32 + kRowParamBytes;              // a group's descriptor and one row's params
 constexpr int kBmEpiWarp0 = 1 + kBmAcc;                     // first epilogue warp; warp 0 is the stager
 constexpr int kRecordWarps = 8;
 static_assert(kBmStages % kBmAcc == 0 && kQPer >= 2, "each issuer owns at least two query stages");
@@ -53,13 +54,13 @@ struct BmLayout {  // offsets from the 1024-byte aligned base of dynamic shared 
   static constexpr uint32_t q = 2 * kWindowBytes;                         // kBmStages x 16 KB
   static constexpr uint32_t window_sf = q + kBmStages * 2 * kQRowBytes;   // 2 x 512 B
   static constexpr uint32_t sf_one = window_sf + 2 * 512;                 // 512 B of 0x7F
-  static constexpr uint32_t prm = sf_one + 512;                           // kBmAcc x kPrmPer x kParamBytes
-  static constexpr uint32_t bars = prm + kBmAcc * kPrmPer * kParamBytes;
+  static constexpr uint32_t prm = sf_one + 512;                           // kEpiWarps x kPrmPer x kSlotBytes
+  static constexpr uint32_t bars = prm + kEpiWarps * kPrmPer * kSlotBytes;
   static constexpr int nbars = 4 + 2 * kBmStages + 3 * kBmAcc;
   static constexpr uint32_t misc = bars + nbars * 8;                      // TMEM address, abort flag
   static constexpr uint32_t bytes = misc + 16;
 };
-static_assert(BmLayout::prm % 16 == 0 && kParamBytes % 16 == 0 && kRowParamBytes % 16 == 0,
+static_assert(BmLayout::prm % 16 == 0 && kSlotBytes % 16 == 0 && kRowParamBytes % 16 == 0,
               "16-byte aligned params");
 static_assert(BmLayout::bars % 8 == 0, "mbarriers are 8-byte aligned");
 static_assert(kBmAcc * kBmN + 12 * kBmAcc <= 512, "accumulators, each issuer's window and query scales fit in TMEM");
@@ -160,9 +161,10 @@ __global__ void __launch_bounds__(kRecordWarps * 32) bm_records_kernel(const __g
 }
 
 // Groups of two records per window, windows in position order: cursor[P]
-// becomes the first record slot of window P (2 x its first group). Positions
-// go in tiles of kScanTile: one kernel sums each tile's groups, the next gives
-// each tile its offset (the sum of the tiles before it) and scans the tile.
+// becomes the first record slot of window P (2 x its first group), and
+// cnt[P] the window's ordinal. Positions go in tiles of kScanTile: one kernel
+// sums each tile's groups and windows, the next gives each tile its offsets
+// (the sums of the tiles before it) and scans the tile.
 // Thread t of a tile takes its positions 8 t .. 8 t + 7 (two 16-byte loads).
 constexpr int kScanThreads = 256;
 constexpr int kScanTile = 8 * kScanThreads;
@@ -212,46 +214,73 @@ __global__ void __launch_bounds__(kScanThreads) bm_tilesum_kernel(const __grid_c
   __shared__ int wsum[33];
   int c[8];
   load_tile_counts(p.cnt, p.total_len, static_cast<int64_t>(blockIdx.x) * kScanTile + 8 * threadIdx.x, c);
-  int mine = 0;
+  int groups = 0, windows = 0;
 #pragma unroll
-  for (int x = 0; x < 8; ++x) mine += (c[x] + 1) >> 1;
-  int total;
-  block_exclusive_scan(mine, wsum, &total);
-  if (threadIdx.x == 0) p.tile_groups[blockIdx.x] = total;
+  for (int x = 0; x < 8; ++x) {
+    groups += (c[x] + 1) >> 1;
+    windows += c[x] > 0 ? 1 : 0;
+  }
+  int total_g, total_w;
+  block_exclusive_scan(groups, wsum, &total_g);
+  __syncthreads();
+  block_exclusive_scan(windows, wsum, &total_w);
+  if (threadIdx.x == 0) {
+    p.tile_groups[blockIdx.x] = total_g;
+    p.tile_windows[blockIdx.x] = total_w;
+  }
 }
 
 __global__ void __launch_bounds__(kScanThreads) bm_plan_kernel(const __grid_constant__ BmIndexParams p) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ int wsum[33];
-  __shared__ int red[kScanThreads / 32];
+  __shared__ int red[2][kScanThreads / 32];
   const int b = blockIdx.x;
-  // this tile's offset: the groups of the tiles before it
-  int before = 0;
-  for (int i = threadIdx.x; i < b; i += kScanThreads) before += p.tile_groups[i];
+  // this tile's offsets: the groups and the windows of the tiles before it
+  int before_g = 0, before_w = 0;
+  for (int i = threadIdx.x; i < b; i += kScanThreads) {
+    before_g += p.tile_groups[i];
+    before_w += p.tile_windows[i];
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(kAll, before, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = before;
+  for (int o = 16; o > 0; o >>= 1) {
+    before_g += __shfl_xor_sync(kAll, before_g, o);
+    before_w += __shfl_xor_sync(kAll, before_w, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = before_g;
+    red[1][threadIdx.x >> 5] = before_w;
+  }
   int c[8];
   const int64_t i0 = static_cast<int64_t>(b) * kScanTile + 8 * threadIdx.x;
   load_tile_counts(p.cnt, p.total_len, i0, c);
-  int mine = 0;
+  int groups = 0, windows = 0;
 #pragma unroll
-  for (int x = 0; x < 8; ++x) mine += (c[x] + 1) >> 1;
-  int total;
-  int g = block_exclusive_scan(mine, wsum, &total);  // its __syncthreads also publish red[]
-  int offset = 0;
+  for (int x = 0; x < 8; ++x) {
+    groups += (c[x] + 1) >> 1;
+    windows += c[x] > 0 ? 1 : 0;
+  }
+  int total_g, total_w;
+  int g = block_exclusive_scan(groups, wsum, &total_g);  // its __syncthreads also publish red[]
+  __syncthreads();
+  int w = block_exclusive_scan(windows, wsum, &total_w);
+  int offset_g = 0, offset_w = 0;
 #pragma unroll
-  for (int w = 0; w < kScanThreads / 32; ++w) offset += red[w];
-  g += offset;
+  for (int x = 0; x < kScanThreads / 32; ++x) {
+    offset_g += red[0][x];
+    offset_w += red[1][x];
+  }
+  g += offset_g;
+  w += offset_w;
 #pragma unroll
   for (int x = 0; x < 8; ++x) {
     if (c[x] == 0) continue;
     p.cursor[i0 + x] = 2 * g;
+    p.cnt[i0 + x] = w++;  // the count is read; the position now keeps its window's ordinal
     if (c[x] & 1) p.groups[g + (c[x] >> 1)].row[1] = -1;  // the window's last group holds one record
     g += (c[x] + 1) >> 1;
   }
-  if (b == gridDim.x - 1 && threadIdx.x == 0) *p.ngroups = offset + total;
+  if (b == gridDim.x - 1 && threadIdx.x == 0) *p.ngroups = offset_g + total_g;
 }
 
 __global__ void __launch_bounds__(kRecordWarps * 32) bm_fill_kernel(const __grid_constant__ BmIndexParams p) {
@@ -268,7 +297,10 @@ __global__ void __launch_bounds__(kRecordWarps * 32) bm_fill_kernel(const __grid
     const int at = atomicAdd(p.cursor + rc.x, 1);
     BmGroup* g = p.groups + (at >> 1);
     const int s = at & 1;
-    if (s == 0) g->P = rc.x;
+    if (s == 0) {
+      g->P = rc.x;
+      g->wo = p.cnt[rc.x];  // the plan kernel left the window's ordinal there
+    }
     g->row[s] = r;
     g->c0m[s] = rc.y;
     g->end[s] = e;
@@ -279,13 +311,14 @@ __global__ void __launch_bounds__(kRecordWarps * 32) bm_fill_kernel(const __grid
 // Score
 // ---------------------------------------------------------------------------
 
-// Warps: 0 window loader, 1..3 MMA issuers, 4..15 epilogue (three
-// warpgroups). Issuer t and epilogue warpgroup t own accumulator t and take
-// the groups it = t, t + 3, ...; issuer t also loads the query tiles of its
-// groups into its own kQPer stages, and warpgroup t fetches their params
-// into its own ring. So every barrier has one waiter that sees its phases in
-// order (a parity wait cannot match a phase two back), except the windows',
-// which every issuer waits for in order.
+// Warps: 0 window loader, 1..3 MMA issuers, 4..27 epilogue (six warpgroups).
+// Issuer t and epilogue warpgroups 2t (row 0 of each group) and 2t + 1 (row
+// 1) own accumulator t and take the groups it = t, t + 3, ...; issuer t also
+// loads the query tiles of its groups into its own kQPer stages, and every
+// epilogue warp fetches its row's params into a ring of its own. So every
+// barrier has one waiter set that sees its phases in order (a parity wait
+// cannot match a phase two back), except the windows', which every issuer
+// waits for in order.
 __global__ void __launch_bounds__(kBmThreads, 1)
     bm_score_kernel(const __grid_constant__ BmScoreParams p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_kw) {
@@ -318,7 +351,7 @@ __global__ void __launch_bounds__(kBmThreads, 1)
     }
     for (int a = 0; a < NA; ++a) {
       mbar_init(acc_full(a), 1);
-      mbar_init(acc_empty(a), 4);  // the warpgroup of accumulator a
+      mbar_init(acc_empty(a), 8);  // the two warpgroups of accumulator a
       mbar_init(bar_drain(a), 1);
     }
     *abort_flag = 0;
@@ -403,34 +436,42 @@ __global__ void __launch_bounds__(kBmThreads, 1)
   } else if (warp <= NA) {
     // ======================= MMA issuers =======================
     // Issuing tcgen05 instructions costs a thread about as much as they take
-    // to run, so three threads share it. Issuer t follows the window sequence
-    // of all groups (the descriptors come from the group list in global
-    // memory, batches of 32 one batch ahead) and keeps its own scale columns;
-    // a window's slot is free once every issuer committed past it. A window
-    // an issuer has no group in is committed after it has loaded (so that a
-    // commit for the slot's next window cannot pass it). For its own group k
-    // it first loads the query tiles of its group k + kQPer - 1 into stage
+    // to run, so three threads share it; each shares its scheduler with six
+    // epilogue warps, so its work per group is kept to a few instructions.
+    // Issuer t takes the groups it = t, t + 3, ... (its own groups k = 0, 1,
+    // ...); lane l holds the descriptor head (P, row0, row1, window ordinal)
+    // of own group base + l, for two alternating batches of 32, each loaded
+    // a batch ahead. Each issuer keeps its own scale columns; a window's slot
+    // is free once every issuer committed past it. A window an issuer has no
+    // group in is committed after it has loaded (so that a commit for the
+    // slot's next window cannot pass it). After the MMAs of own group k it
+    // loads the query tiles of own group k + kQPer - 1 into stage
     // (k + kQPer - 1) % kQPer of its own. Lane 0 issues.
     const int t = warp - 1;
     const uint32_t sfa = tm_sfa + 8 * t, sfb = tm_sfb + 4 * t;
     uint32_t idesc[4];
     for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kTypeE2M1, kTypeE4M3, 128, kBmN, g, g);
     if (lane == 0) tmem_cp_32x128b_x4(sfb, rows16_desc(smem_addr(sf_one)));
+    const int own = n > t ? (n - t + NA - 1) / NA : 0;
+    const int wo0 = n > 0 ? groups[0].wo : 0;               // the range's first window ordinal
+    const int nwin = n > 0 ? groups[n - 1].wo - wo0 + 1 : 0;  // windows of the range
     bool ok = true;
-    int cur = -1, nw = 0;  // window id and count over the groups scanned so far
-    int mine = -1;         // the window this issuer is in
-    int scan = 0;          // next group to scan for a window change
-    int issued = 0;        // own groups whose query tiles are out
-    int base = 0;
-    auto load4 = [&](int b) {
-      return b + lane < n ? *reinterpret_cast<const int4*>(groups + b + lane) : make_int4(-1, -1, -1, 0);
+    int mine = -1;    // the window this issuer is in
+    int issued = 0;   // own groups whose query tiles are out
+    auto head = [&](int k) {  // descriptor head of own group k
+      return k < own ? *reinterpret_cast<const int4*>(groups + t + NA * k) : make_int4(0, -1, -1, 0);
     };
-    int4 dcur = load4(0), dnxt = load4(32);  // (P, row0, row1, c0m0) of groups base + lane, base + 32 + lane
-    auto field = [&](int g, int f) {         // field f of group g, base <= g < base + 64 (g uniform)
-      const int d = g - base;
-      const int4 src = d < 32 ? dcur : dnxt;
-      const int v = f == 0 ? src.x : (f == 1 ? src.y : src.z);
-      return __shfl_sync(kAll, v, d & 31);
+    int4 hcur = head(lane), hnxt = head(32 + lane);
+    int base = 0;  // own group of hcur's lane 0
+    auto get = [&](int k) {  // own group k's head, base <= k < base + 64 (k uniform)
+      const int d = k - base;
+      const int4 h = d < 32 ? hcur : hnxt;
+      int4 r;
+      r.x = __shfl_sync(kAll, h.x, d & 31);
+      r.y = __shfl_sync(kAll, h.y, d & 31);
+      r.z = __shfl_sync(kAll, h.z, d & 31);
+      r.w = __shfl_sync(kAll, h.w, d & 31);
+      return r;
     };
     auto pass_windows = [&](int upto) {  // lane 0: commit windows [max(mine, 0), upto) this issuer leaves
       for (int w = mine < 0 ? 0 : mine; w < upto && ok; ++w) {
@@ -438,42 +479,32 @@ __global__ void __launch_bounds__(kBmThreads, 1)
         mma_commit(win_empty(w & 1));
       }
     };
-    auto load_q = [&](int k) {  // query tiles of own group k (k < count of own groups)
+    auto load_q = [&](int k, int r0, int r1) {  // lane 0: query tiles of own group k
       const int g = t + NA * k;
-      const int r0 = field(g, 1), r1 = field(g, 2);
-      if (lane == 0) {
-        const int s = t * kQPer + k % kQPer;
-        ok = ok && mbar_wait(q_empty(s), ((k / kQPer) & 1) ^ 1, abort_flag, p.wait_ns);
-        if (ok && !(g == p.stall_group && blockIdx.x == 0)) {
-          const uint32_t qdst = smem_addr(smem + L::q + s * 2 * kQRowBytes);
-          mbar_arrive_expect_tx(q_full(s), (r1 >= 0 ? 2 : 1) * kQRowBytes);
-          tma_load_2d(qdst, &tm_q, 0, r0 * kBmHeads, q_full(s));
-          if (r1 >= 0) tma_load_2d(qdst + kQRowBytes, &tm_q, 0, r1 * kBmHeads, q_full(s));
-        }
+      const int s = t * kQPer + k % kQPer;
+      ok = ok && mbar_wait(q_empty(s), ((k / kQPer) & 1) ^ 1, abort_flag, p.wait_ns);
+      if (ok && !(g == p.stall_group && blockIdx.x == 0)) {
+        const uint32_t qdst = smem_addr(smem + L::q + s * 2 * kQRowBytes);
+        mbar_arrive_expect_tx(q_full(s), (r1 >= 0 ? 2 : 1) * kQRowBytes);
+        tma_load_2d(qdst, &tm_q, 0, r0 * kBmHeads, q_full(s));
+        if (r1 >= 0) tma_load_2d(qdst + kQRowBytes, &tm_q, 0, r1 * kBmHeads, q_full(s));
       }
-      ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
       issued = k + 1;
     };
-    const int own = n > t ? (n - t + NA - 1) / NA : 0;  // own groups
-    for (int k = 0; k < kQPer - 1 && k < own && ok; ++k) load_q(k);
-    for (int k = 0; k < own && ok; ++k) {
-      const int it = t + NA * k;
-      for (; scan <= it; ++scan) {  // window changes of every group up to this one
-        const int P = field(scan, 0);
-        if (P != cur) {
-          cur = P;
-          ++nw;
-        }
-      }
-      if (it >= base + 32) {  // slide the descriptor batches: the next one was loaded a batch ago
+    for (int k = 0; k < kQPer - 1 && k < own; ++k) {
+      const int4 h = get(k);
+      if (lane == 0) load_q(k, h.y, h.z);
+    }
+    for (int k = 0; k < own; ++k) {
+      if (k >= base + 32) {  // slide the batches: the next one was loaded a batch ago
         base += 32;
-        dcur = dnxt;
-        dnxt = load4(base + 32);
+        hcur = hnxt;
+        hnxt = head(base + 32 + lane);
       }
-      if (k + kQPer - 1 < own) load_q(k + kQPer - 1);
-      if (!ok) break;
-      if (lane == 0) {
-        const int wi = nw - 1;
+      const int4 h = get(k);
+      const int4 hq = get(k + kQPer - 1 < own ? k + kQPer - 1 : k);
+      if (lane == 0 && ok) {
+        const int wi = h.w - wo0;
         if (wi != mine) {
           pass_windows(wi);
           ok = ok && mbar_wait(win_full(wi & 1), (wi >> 1) & 1, abort_flag, p.wait_ns);
@@ -496,22 +527,16 @@ __global__ void __launch_bounds__(kBmThreads, 1)
             mma_mxf8f6f4(tmem + t * kBmN, adesc + 2 * g, bdesc + 2 * g, idesc[g], sfa + 4 * slot, sfb, g > 0);
           mma_commit(acc_full(t));
           mma_commit(q_empty(s));
+          // the query tiles of own group k + kQPer - 1, into the stage of
+          // group k - 1: after this group's MMAs are out, so that waiting for
+          // the previous group's MMAs to finish overlaps this group's
+          if (k + kQPer - 1 < own) load_q(k + kQPer - 1, hq.y, hq.z);
         }
       }
-      ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+      if (__shfl_sync(kAll, ok ? 1 : 0, 0) == 0) break;
     }
     if (lane == 0) {
-      if (ok) {  // the windows left: this issuer's last and those with none of its groups
-        for (; scan < n; ++scan) {
-          // the remaining groups' window ids, read directly (lane 0 alone)
-          const int P = groups[scan].P;
-          if (P != cur) {
-            cur = P;
-            ++nw;
-          }
-        }
-        pass_windows(nw);
-      }
+      if (ok) pass_windows(nwin);  // the windows left: this issuer's last and those with none of its groups
       if (!ok) {
         status_or(p.status, kStatusTimeout);
         *abort_flag = 1;
@@ -524,112 +549,84 @@ __global__ void __launch_bounds__(kBmThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= epilogue (warps 4..15) =======================
-    // Warpgroup t takes the groups it = t, t + 3, ... whole (both rows), so
-    // that the warps sharing a scheduler are at different points of different
-    // groups. It fetches each group's descriptor and its rows' params itself,
-    // one group ahead, by 16-byte asynchronous copies (one per thread) into a
-    // ring of kPrmPer slots of its own; the rows of the group after that come
-    // from a load two groups ahead. A named barrier per warpgroup publishes
-    // the copies and frees the slots.
-    const int wg = (warp - kBmEpiWarp0) >> 2;
-    const int wt = tid - 32 * (kBmEpiWarp0 + 4 * wg);  // thread of the warpgroup
-    const int q4 = warp & 3;        // TMEM lane quarter
-    const int m = 32 * q4 + lane;   // key of the window
+    // ======================= epilogue (warps 4..27) =======================
+    // Warpgroups 2t and 2t + 1 take the groups it = t, t + 3, ..., one row
+    // each: so an accumulator goes back after one round of loads and half a
+    // row's arithmetic. Each warp fetches each group's descriptor and its
+    // row's params itself, one group ahead, by 16-byte asynchronous copies
+    // into a ring of kPrmPer slots of its own (no barrier across warps); the
+    // rows of the group after that come from a load two groups ahead.
+    const int ew = warp - kBmEpiWarp0;  // epilogue warp: its ring
+    const int a = ew >> 3;              // accumulator (and issuer) of its groups
+    const int e = (ew >> 2) & 1;        // its row of each group
+    const int q4 = warp & 3;            // TMEM lane quarter
+    const int m = 32 * q4 + lane;       // key of the window
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     const int shift = 31 - __clz(p.sbkv);
     const int sl = m >> shift;
     const uint32_t below = (1u << sl) - 1u;
     const int moff = m & (p.sbkv - 1);
-    const int own = n > wg ? (n - wg + NA - 1) / NA : 0;
-    constexpr int kChunks = (kParamBytes + 15) / 16;  // 36: descriptor, then the two rows' params
-    static_assert(kChunks <= 128, "one chunk per thread of the warpgroup");
-    auto fetch = [&](int k, int r0, int r1) {  // group k's descriptor and params into slot k % kPrmPer
-      if (k < own && wt < kChunks) {
-        const uint32_t dst = smem_addr(smem + L::prm + (wg * kPrmPer + k % kPrmPer) * kParamBytes) + 16 * wt;
-        const uint8_t* src;
-        if (wt < 2) {
-          src = reinterpret_cast<const uint8_t*>(groups + wg + NA * k) + 16 * wt;
-        } else {
-          const int c = wt - 2, e = c / (kRowParamBytes / 16), off = c % (kRowParamBytes / 16);
-          const int r = e == 0 ? r0 : r1;
-          src = reinterpret_cast<const uint8_t*>(p.rowparams + static_cast<int64_t>(r < 0 ? r0 : r) * kBmRowParams) + 16 * off;
-        }
+    const int own = n > a ? (n - a + NA - 1) / NA : 0;
+    constexpr int kChunks = kSlotBytes / 16;  // 19: descriptor, then the row's params
+    static_assert(kChunks <= 32, "one chunk per lane");
+    auto fetch = [&](int k, int r) {  // group k's descriptor and row params into slot k % kPrmPer
+      if (k < own && lane < kChunks) {
+        const uint32_t dst = smem_addr(smem + L::prm + (ew * kPrmPer + k % kPrmPer) * kSlotBytes) + 16 * lane;
+        const uint8_t* src =
+            lane < 2 ? reinterpret_cast<const uint8_t*>(groups + a + NA * k) + 16 * lane
+                     : reinterpret_cast<const uint8_t*>(p.rowparams + static_cast<int64_t>(r < 0 ? 0 : r) * kBmRowParams) +
+                           16 * (lane - 2);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    auto rows_of = [&](int k) {  // (row0, row1) of group k, or (-1, -1)
-      if (k >= own) return make_int2(-1, -1);
-      const int4 d = *reinterpret_cast<const int4*>(groups + wg + NA * k);
-      return make_int2(d.y, d.z);
+    auto row_of = [&](int k) {  // this warp's row of group k, or -1
+      if (k >= own) return -1;
+      const int4 d = *reinterpret_cast<const int4*>(groups + a + NA * k);  // (P, row0, row1, c0m0)
+      return e == 0 ? d.y : d.z;
     };
-    int2 r1n = rows_of(1);  // rows of the next group
-    {
-      const int2 r0n = rows_of(0);
-      fetch(0, r0n.x, r0n.y);
-    }
+    int r1n = row_of(1);  // the next group's row
+    fetch(0, row_of(0));
     bool ok = true;
     for (int k = 0; k < own && ok; ++k) {
-      const int2 r2n = rows_of(k + 2);  // used next step
-      fetch(k + 1, r1n.x, r1n.y);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's copies of group k
-      const int a = wg;
-      ok = warp_wait(acc_full(a), k & 1, abort_flag, p.wait_ns);
-      // every thread's copies of group k are in, slot k - 1 is read; and the
-      // warpgroup agrees on going on (a wait that gave up stops all four warps)
-      uint32_t all_ok;
-      asm volatile(
-          "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, %2, 128, pi;\n"
-          " selp.u32 %0, 1, 0, po;\n}"
-          : "=r"(all_ok)
-          : "r"(ok ? 1u : 0u), "r"(1 + wg)
-          : "memory");
-      ok = all_ok != 0;
+      const int r2n = row_of(k + 2);  // used next step
+      fetch(k + 1, r1n);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this lane's copies of group k
+      ok = warp_wait(acc_full(a), k & 1, abort_flag, p.wait_ns);  // its __syncwarp also publishes the lanes' copies
       if (!ok) break;
       tc_fence_after();
-      const uint8_t* prm = smem + L::prm + (wg * kPrmPer + k % kPrmPer) * kParamBytes;
+      const uint8_t* prm = smem + L::prm + (ew * kPrmPer + k % kPrmPer) * kSlotBytes;
       const BmGroup* gd = reinterpret_cast<const BmGroup*>(prm);
-      const int row0 = gd->row[0], row1 = gd->row[1];
-      // Both rows in two halves of 32 heads: the second half's loads are the
-      // last reads of the accumulator, so it goes back before half of the
-      // arithmetic. Per row, heads h = 0, 1 (mod 4) accumulate in lo and
+      const int row = gd->row[e];
+      // Two halves of 32 heads: the second half's loads are this warp's last
+      // reads of the accumulator. Heads h = 0, 1 (mod 4) accumulate in lo and
       // h = 2, 3 (mod 4) in hi, each in head order.
-      float2 lo[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float2 hi[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        uint32_t v[64];  // row 0 heads 32 half .. + 31, then row 1's
-        const uint32_t tacc = tmem + a * kBmN + 32 * half + lane_base;
+        uint32_t v[32];
+        const uint32_t tacc = tmem + a * kBmN + e * kBmHeads + 32 * half + lane_base;
         tmem_ld16(tacc, *reinterpret_cast<uint32_t(*)[16]>(v));
         tmem_ld16(tacc + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-        tmem_ld16(tacc + kBmHeads, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
-        tmem_ld16(tacc + kBmHeads + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
         tmem_wait_ld();
-        if (half == 1) {  // every column of the accumulator is in registers: hand it back
+        if (half == 1) {  // this warp's columns are in registers: its share of the hand-back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty(a));
         }
+        if (row < 0) continue;
+        const float4* w4 = reinterpret_cast<const float4*>(prm + 32) + 8 * half;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (e == 1 && row1 < 0) break;
-          const float4* w4 = reinterpret_cast<const float4*>(prm + 32 + e * kRowParamBytes) + 8 * half;
-#pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 w = w4[h4];
-            const uint32_t* x = v + 32 * e + 4 * h4;
-            fma2(lo[e], w.x, w.y, fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
-            fma2(hi[e], w.z, w.w, fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
-          }
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 w = w4[h4];
+          const uint32_t* x = v + 4 * h4;
+          fma2(lo, w.x, w.y, fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
+          fma2(hi, w.z, w.w, fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
         }
       }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int row = e == 0 ? row0 : row1;
-        if (row < 0) continue;
-        const float qs = reinterpret_cast<const float*>(prm + 32 + e * kRowParamBytes)[kBmHeads];
-        const float logit = ((lo[e].x + lo[e].y) + (hi[e].x + hi[e].y)) * qs;
+      if (row >= 0) {
+        const float qs = reinterpret_cast<const float*>(prm + 32)[kBmHeads];
+        const float logit = ((lo.x + lo.y) + (hi.x + hi.y)) * qs;
         const uint32_t c0m = static_cast<uint32_t>(gd->c0m[e]);
         const uint32_t mask = c0m >> 24;
         if ((mask >> sl) & 1u) {
