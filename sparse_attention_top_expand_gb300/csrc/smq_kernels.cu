@@ -412,7 +412,17 @@ struct TopkScratch {
 // CTAs of the same kernel, so they are read from L2.
 // kShared: L and the ids (sm.sidx, sparse_row unused) are already in this
 // CTA's shared memory.
-template <int kThreads, int kJ, bool kWide, bool kShared = false>
+// Value-range first pass (kRange): one block reduction gives the row's
+// minimum and maximum, a 1024-bin histogram over that value range (a
+// monotone map, so every key in a higher bin is strictly greater) finds the
+// bin holding the k-th key, and one warp sorts that bin's keys (at most
+// kRangeBin; key descending, column ascending) to give the exact threshold
+// key and how many keys equal to it are taken. A row whose bin holds more
+// keys (ties, spikes) falls back to the digit passes on the same registers.
+constexpr int kRangeBins = 1024;
+constexpr int kRangeBin = 64;
+
+template <int kThreads, int kJ, bool kWide, bool kShared = false, bool kRange = false>
 __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k, const int32_t* sparse_row, int nsb,
                             int sbkv, int32_t* out, int32_t* colo, float* fill, uint16_t* fill16,
                             const TopkScratch& sm) {
@@ -459,7 +469,160 @@ __device__ void select_topk(const float* L, int S, const int32_t* end_src, int k
   uint32_t prefix = 0;  // selected high bits so far
   int need = k;         // keys still to take among those matching the prefix
   int done_bits = 0;
-  if constexpr (kWide) {
+  bool ranged = false;  // the value-range pass found the threshold
+  if constexpr (kRange) {
+    // -- minimum and maximum of the valid keys
+    float vmin = INFINITY, vmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j)
+      if (tid + j * kThreads < e) {
+        vmin = fminf(vmin, raw[j]);
+        vmax = fmaxf(vmax, raw[j]);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      vmin = fminf(vmin, __shfl_xor_sync(kFullMask, vmin, o));
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, o));
+    }
+    float* red = reinterpret_cast<float*>(hist + kRangeBins + 2 * kRangeBin + 8);  // [2 * kWarps]
+    if (lane == 0) {
+      red[warp] = vmin;
+      red[kWarps + warp] = vmax;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      vmin = fminf(vmin, red[w2]);
+      vmax = fmaxf(vmax, red[kWarps + w2]);
+    }
+    if (!(vmax > vmin) || !(vmax - vmin < INFINITY)) {
+      // every valid key equal (take the first k), or a range too wide for the map: the digit passes decide
+      if (vmin == vmax) {
+        prefix = ordered_key(vmin);
+        done_bits = 32;
+        ranged = true;
+      }
+    } else {
+      const float scale = static_cast<float>(kRangeBins) / (vmax - vmin);
+      auto bin_of = [&](float x) { return static_cast<int>(fminf((x - vmin) * scale, kRangeBins - 1.f)); };
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (tid + j * kThreads < e) atomicAdd(&hist[bin_of(raw[j])], 1u);
+      __syncthreads();
+      // descending scan: thread t owns bins kRangeBins - 1 - per t - b for b < per
+      constexpr int per = (kRangeBins + kThreads - 1) / kThreads;
+      int cnt[per];
+      int local = 0;
+#pragma unroll
+      for (int b = 0; b < per; ++b) {
+        const int bin = kRangeBins - 1 - per * tid - b;
+        cnt[b] = bin >= 0 ? static_cast<int>(hist[bin]) : 0;
+        local += cnt[b];
+      }
+      int incl = local;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+      __syncthreads();
+      int cum = incl - local;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) cum += w2 < warp ? sm.wsum[w2] : 0;
+#pragma unroll
+      for (int b = 0; b < per; ++b) {
+        if (cnt[b] > 0 && cum < need && need <= cum + cnt[b]) {
+          sel_bin[0] = kRangeBins - 1 - per * tid - b;
+          sel_above[0] = cum;
+          sel_cnt[0] = cnt[b];
+        }
+        cum += cnt[b];
+      }
+      uint32_t* list = hist + kRangeBins;  // [kRangeBin] (key, column) of the threshold bin
+      int* list_n = reinterpret_cast<int*>(hist + kRangeBins + 2 * kRangeBin);
+      if (tid == 0) *list_n = 0;
+      __syncthreads();
+      const int tb = sel_bin[0], tcount = sel_cnt[0], above = sel_above[0];
+      if (tcount <= kRangeBin) {
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+          const int c = tid + j * kThreads;
+          if (c < e && bin_of(raw[j]) == tb) {
+            const int at = atomicAdd(list_n, 1);
+            list[2 * at] = ordered_key(raw[j]);
+            list[2 * at + 1] = static_cast<uint32_t>(c);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // bitonic sort of kRangeBin = 64 composites (key, ~column), descending:
+          // lane l holds elements l and l + 32
+          uint64_t x[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            x[h] = i < tcount ? (static_cast<uint64_t>(list[2 * i]) << 32) | (0xFFFFFFFFu - list[2 * i + 1]) : 0ull;
+          }
+#pragma unroll
+          for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                const bool desc = (i & size) == 0;  // this element's block sorts descending
+                if (stride == 32) {
+                  if (h == 0) {  // the pair (i, i + 32) sits in this lane
+                    const bool swap = desc ? (x[0] < x[1]) : (x[0] > x[1]);
+                    if (swap) {
+                      const uint64_t tmp = x[0];
+                      x[0] = x[1];
+                      x[1] = tmp;
+                    }
+                  }
+                } else {
+                  const uint64_t y = __shfl_xor_sync(kFullMask, x[h], stride);
+                  const bool lower = (i & stride) == 0;
+                  const bool take_max = lower == desc;
+                  x[h] = take_max ? (x[h] > y ? x[h] : y) : (x[h] < y ? x[h] : y);
+                }
+              }
+            }
+          }
+          // the (need - above)-th largest is the threshold; how many equal keys are taken
+          const int want = need - above;  // 1 .. tcount
+          const int src = want - 1;
+          const uint64_t tsel = __shfl_sync(kFullMask, x[src >> 5], src & 31);
+          const uint32_t tkey = static_cast<uint32_t>(tsel >> 32);
+          int eq = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            eq += (i < want && static_cast<uint32_t>(x[h] >> 32) == tkey) ? 1 : 0;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) eq += __shfl_xor_sync(kFullMask, eq, o);
+          if (lane == 0) {
+            sel_bin[1] = static_cast<int>(tkey);
+            sel_cnt[1] = eq;
+          }
+        }
+        __syncthreads();
+        prefix = static_cast<uint32_t>(sel_bin[1]);
+        need = sel_cnt[1];
+        done_bits = 32;
+        ranged = true;
+      }
+    }
+    if (!ranged) {  // back to the digit passes: clear what the range pass used
+      __syncthreads();
+      for (int i = tid; i < (kWide ? kTopkBins : 256 * 32) / 4; i += kThreads) hist4[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+  }
+  if (ranged) {
+    // the threshold is known: straight to the compaction
+  } else if constexpr (kWide) {
   for (int pass = 0; pass < 3; ++pass) {
     const int wbits = pass < 2 ? 12 : 8;
     const int nb = 1 << wbits;
@@ -1456,7 +1619,7 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? (kJ <= 8 ? 6 : 4) 
   const int r = blockIdx.x;
   const int S = p.num_cols;
   const TopkScratch sm{hist, bsum, wsum, chunk, sidx, sel};
-  select_topk<kThreads, kJ, false>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
+  select_topk<kThreads, kJ, false, false, true>(p.logits + static_cast<int64_t>(r) * S, S, p.end + r, p.topk,
                                 p.sparse_indices + static_cast<int64_t>(r) * p.nsb, p.nsb, p.sbkv,
                                 p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
                                 p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr,

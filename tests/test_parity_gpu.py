@@ -292,6 +292,24 @@ def test_two_values_many_ties():
     check_rows(inp, dev, plan, oracle.reference_rows(inp, rows=range(8), mode="sparse"))
 
 
+@pytest.mark.parametrize("mode", ["equal", "two_values"])
+def test_prefill_topk_kernel_with_ties(mode):
+    """The separate top-k kernel (prefill rows) on crowded thresholds: every
+    key equal (the value range is a single point) or keys of two values (the
+    threshold bin overflows and the digit passes decide); ties go by column."""
+    inp = synth.prefill_chunk(seed=41, seq_lens=(1500, 2300), queries_per_seq=30, num_heads=64, page_size=64,
+                              cbs=128, ncb=8, topk=300)
+    half = inp.geom.page_size * 64
+    inp.k_cache[:, :half] = 0x22  # every element 1.0
+    if mode == "two_values":
+        inp.k_cache[::3, :half] = 0x44  # every third page 3.0
+    inp.k_cache[:, half:] = 127
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    kv, ks = oracle.gather_reference(inp)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="sparse", contig=(kv, ks)))
+
+
 def test_zero_rows_is_a_no_op():
     inp = synth.tiny_decode(0)
     plan = tensors.plan_for(inp.geom, max_rows=4)
