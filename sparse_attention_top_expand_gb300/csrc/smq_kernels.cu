@@ -295,59 +295,71 @@ __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_
 
 // The same with the row's candidates already loaded: lane l holds ids l (c0)
 // and l + 32 (c1), -1 past the row's ncb.
+// The ids that are in range go through a bitonic sorting network across the
+// warp (one id per lane, or two for more than 32 candidates; out-of-range ids
+// sort last as INT_MAX). A sorted id equal to its predecessor is a repeat and is
+// dropped; the rest land in `sorted` at their rank, counted by ballots. Block b
+// holds min(cbs, L - b cbs) columns below L.
 __device__ int expand_row_in_warp(const ScoreParams& p, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
                                    int lane) {
   const int ncb = p.ncb;
+  const int64_t cbs = p.cbs;
+  auto key = [&](int b, bool live) { return live && b >= 0 && static_cast<int64_t>(b) * cbs < L ? b : INT_MAX; };
+  auto block_cols = [&](int b, bool keep) {
+    const int64_t rest = keep ? L - static_cast<int64_t>(b) * cbs : 0;
+    return static_cast<int>(rest < cbs ? rest : cbs);
+  };
+  int v0 = key(c0, lane < ncb);
+  int v1 = key(c1, lane + 32 < ncb);
   const uint32_t lt = (1u << lane) - 1u;
-  auto in_range = [&](int b) { return b >= 0 && static_cast<int64_t>(b) * p.cbs < L; };
-  // first occurrence: no lower lane (and for c1 no c0 at all) holds the same id.
-  // Every lane takes part in each warp vote, so the votes come first and the
-  // per-lane conditions after them.
-  const uint32_t same0 = __match_any_sync(kFullMask, c0);
-  const bool keep0 = lane < ncb && in_range(c0) && (same0 & lt) == 0;
-  bool keep1 = false;
-  if (ncb > 32) {
-    const uint32_t same1 = __match_any_sync(kFullMask, c1);
-    bool dup = (same1 & lt) != 0;
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) dup |= __shfl_sync(kFullMask, c0, j) == c1;
-    keep1 = lane + 32 < ncb && in_range(c1) && !dup;
+  if (ncb <= 32) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int o = __shfl_xor_sync(kFullMask, v0, j);
+        v0 = (((lane & k) == 0) == ((lane & j) == 0)) ? min(v0, o) : max(v0, o);
+      }
+    const int prev = __shfl_up_sync(kFullMask, v0, 1);
+    const bool keep = v0 != INT_MAX && (lane == 0 || prev != v0);
+    const uint32_t bal = __ballot_sync(kFullMask, keep);
+    if (keep) sorted[__popc(bal & lt)] = v0;
+    const int cols = __reduce_add_sync(kFullMask, block_cols(v0, keep));
+    __syncwarp();
+    *nkept_out = __popc(bal);
+    return cols;
   }
-  const int k0 = keep0 ? c0 : INT_MAX, k1 = keep1 ? c1 : INT_MAX;
-  int rank0 = 0, rank1 = 0;
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) {
-    const int a = __shfl_sync(kFullMask, k0, j);
-    rank0 += a < k0;
-    rank1 += a < k1;
-  }
-  if (ncb > 32) {
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-      const int b = __shfl_sync(kFullMask, k1, j);
-      rank0 += b < k0;
-      rank1 += b < k1;
+  // 64 entries: entry i is (lane i % 32, register i / 32)
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // partners in the same lane
+        const int a = min(v0, v1), b = max(v0, v1);
+        v0 = a;
+        v1 = b;
+      } else {
+        const int o0 = __shfl_xor_sync(kFullMask, v0, j);
+        const int o1 = __shfl_xor_sync(kFullMask, v1, j);
+        const bool lower = (lane & j) == 0;
+        const bool up0 = k == 64 || (lane & k) == 0;
+        const bool up1 = k == 64 || (k < 32 && (lane & k) == 0);
+        v0 = (up0 == lower) ? min(v0, o0) : max(v0, o0);
+        v1 = (up1 == lower) ? min(v1, o1) : max(v1, o1);
+      }
     }
-  }
-  const int nkept = __popc(__ballot_sync(kFullMask, keep0)) + __popc(__ballot_sync(kFullMask, keep1));
-  if (keep0) sorted[rank0] = c0;
-  if (keep1) sorted[rank1] = c1;
-  const int sbkv = p.sbkv, spb = p.cbs / p.sbkv;
-  int64_t cols = 0;
-  for (int u = 0; u < spb; ++u) {
-    if (keep0) {
-      const int64_t start = (static_cast<int64_t>(c0) * spb + u) * sbkv;
-      if (start < L) cols += L - start < sbkv ? L - start : sbkv;
-    }
-    if (keep1) {
-      const int64_t start = (static_cast<int64_t>(c1) * spb + u) * sbkv;
-      if (start < L) cols += L - start < sbkv ? L - start : sbkv;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) cols += __shfl_xor_sync(kFullMask, cols, o);
+  const int p0 = __shfl_up_sync(kFullMask, v0, 1);
+  const int p1 = __shfl_up_sync(kFullMask, v1, 1);
+  const int last0 = __shfl_sync(kFullMask, v0, 31);
+  const bool keep0 = v0 != INT_MAX && (lane == 0 || p0 != v0);
+  const bool keep1 = v1 != INT_MAX && (lane == 0 ? last0 != v1 : p1 != v1);
+  const uint32_t b0 = __ballot_sync(kFullMask, keep0), b1 = __ballot_sync(kFullMask, keep1);
+  if (keep0) sorted[__popc(b0 & lt)] = v0;
+  if (keep1) sorted[__popc(b0) + __popc(b1 & lt)] = v1;
+  const int cols = __reduce_add_sync(kFullMask, block_cols(v0, keep0) + block_cols(v1, keep1));
   __syncwarp();
-  *nkept_out = nkept;
-  return static_cast<int>(cols);
+  *nkept_out = __popc(b0) + __popc(b1);
+  return cols;
 }
 
 // The expansion of row r (sorted[0 .. nkept), `cols` columns below L) to
@@ -939,6 +951,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // sub-block to its page. Tiles past the row's end are published empty.
     const int tiles_per_batch = 32 / spt;
     const int spb = p.cbs / sbkv;
+    const int spp = p.page_size / sbkv;  // sub-blocks per cache page
     int32_t* sorted = reinterpret_cast<int32_t*>(smem + lay.sched);
     int32_t* rend = reinterpret_cast<int32_t*>(smem + lay.rend);
     const int r_first = find_row(prefix, R, t_begin);
@@ -970,12 +983,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const uint8_t* vsrc = nullptr;
         const uint8_t* ssrc = nullptr;
         const bool want = t < tz && col_sub * sbkv < e;  // columns below end are valid sub-blocks
-        int64_t tpos = 0;
+        int tok = 0;
         int pg = -1;
         if (want) {
           const int sb = sorted[col_sub / spb] * spb + col_sub % spb;
-          tpos = static_cast<int64_t>(sb) * sbkv;
-          const int64_t slot = tpos / p.page_size;
+          const int slot = sb / spp;
+          tok = (sb - slot * spp) * sbkv;
           if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
             pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
         }
@@ -985,11 +998,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         if (want) {
           if (pg >= 0 && pg < p.num_pages) {
-            const int64_t tok = tpos % p.page_size;
             const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
             vsrc = base + tok * (kHeadDim / 2);
-            ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
-            trow = static_cast<int>(tok);
+            ssrc = base + p.page_size * (kHeadDim / 2) + tok * kScaleWordBytes;
+            trow = tok;
             tpage = pg;
             ntok = sbkv;
           } else {
@@ -1049,16 +1061,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           bool valid = false;
           if (sb >= 0) {
             if constexpr (kPaged) {
-              const int64_t tpos = static_cast<int64_t>(sb) * sbkv;
-              const int64_t slot = tpos / p.page_size;
+              const int spp = p.page_size / sbkv;
+              const int slot = sb / spp;
               if (brow >= 0 && brow < p.bt_rows && slot < p.bt_stride) {
                 const int pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
                 if (pg >= 0 && pg < p.num_pages) {
-                  const int64_t tok = tpos % p.page_size;
+                  const int tok = (sb - slot * spp) * sbkv;
                   const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
                   vsrc = base + tok * (kHeadDim / 2);
-                  ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
-                  trow = static_cast<int>(tok);
+                  ssrc = base + p.page_size * (kHeadDim / 2) + tok * kScaleWordBytes;
+                  trow = tok;
                   tpage = pg;
                   ntok = sbkv;
                   valid = true;
@@ -1720,7 +1732,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint8_t* smem = align1024(rc_smem_raw);
   constexpr int NS = kScoreStages;
   constexpr int NA = acc_buffers(kN);
-  constexpr int kWarps = kScoreThreads / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = p.cluster;
   const int r = blockIdx.x / C;
@@ -1860,10 +1871,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int64_t L = s_ke > 0 ? s_ke : 0;
     const int brow = s_brow;
     const int spb = p.cbs / sbkv;
+#ifdef SMQ_TRACE
+    if (__shfl_sync(kFullMask, s_c0 ^ s_c1 ^ s_ke ^ s_brow, 0) != 0x5a5a5a5a && lane == 0) SMQ_MARK(17);
+#endif
     int e = 0;
     if (p.fused) {
       int nkept = 0;
       const int cols = expand_row_in_warp(p, L, s_c0, s_c1, sorted, &nkept, lane);
+      if (lane == 0) SMQ_MARK(18);
       e = cols < 0 ? 0 : (cols > S ? S : cols);
       for (int slot = lane; slot < p.nsb; slot += 32) {
         const int k = slot / spb;
@@ -1886,17 +1901,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     bool ok = true;
     int it = 0;
     const int tiles_per_batch = 32 / spt;
+    const int spp = p.page_size / sbkv;  // sub-blocks per cache page
     for (int tb = 0; tb < n && ok; tb += tiles_per_batch) {
       const int tl = tb + lane / spt;  // local tile
       const int sub = lane % spt;
       const int col_sub = (t0 + tl) * spt + sub;
       const bool want = tl < n && col_sub * sbkv < e;
-      int pg = -1;
-      int64_t tpos = 0;
+      int pg = -1, tok = 0;
       if (want) {
-        tpos = static_cast<int64_t>(sidx[col_sub]) * sbkv;
-        const int64_t slot = tpos / p.page_size;
-        if (sidx[col_sub] >= 0 && brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
+        const int sb = sidx[col_sub];
+        const int slot = sb / spp;
+        tok = (sb - slot * spp) * sbkv;
+        if (sb >= 0 && brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
           pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
       }
       if (owner) {
@@ -1910,11 +1926,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint8_t* ssrc = nullptr;
       if (want) {
         if (pg >= 0 && pg < p.num_pages) {
-          const int64_t tok = tpos % p.page_size;
           const uint8_t* base = p.k_cache + static_cast<int64_t>(pg) * p.page_bytes;
           vsrc = base + tok * (kHeadDim / 2);
-          ssrc = base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) + tok * kScaleWordBytes;
-          trow = static_cast<int>(tok);
+          ssrc = base + p.page_size * (kHeadDim / 2) + tok * kScaleWordBytes;
+          trow = tok;
           tpage = pg;
           ntok = sbkv;
         } else {
@@ -1966,6 +1981,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       uint32_t idesc[4];
       for (int g = 0; g < 4; ++g) idesc[g] = mxf8f6f4_idesc(kE2M1, kE4M3, kMmaM, kN, g, g);
       bool ok = mbar_wait(bar_q_full, 0, abort_flag, static_cast<uint64_t>(p.wait_ns));
+      if (warp == 1) SMQ_MARK(20);
       const uint64_t bdesc = sw128_desc(smem_addr(smem + lay.q));
       for (int it = 0; it < n && ok; ++it) {
         if (NA > 1 ? ((it & 1) != par) : (par != 0)) continue;
@@ -2141,6 +2157,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
         }
+        if (warp == 6 && lane == 0 && i0 == 0) SMQ_MARK(19);
         load_tile(v[0], sw[0], i0);
         if (i0 + 1 < n) {
           if (!both) {
@@ -2192,6 +2209,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   };
   const bool select = e > k;
   cluster_wait();  // every CTA of the cluster has initialised its barriers
+  if (tid == 0) SMQ_MARK(21);
   if (rank != 0) {
     if (select) {
       const int nv = valid_cols(rank);
