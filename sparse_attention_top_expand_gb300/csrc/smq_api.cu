@@ -222,6 +222,7 @@ int run_expand(const smq_plan* p, const int32_t* cand, const int32_t* ks, const 
 int run_topk(const smq_plan* p, const CommonRows& a, const smq::ScoreParams& s, cudaStream_t stream) {
   smq::TopkParams t;
   t.rows = a.rows;
+  t.num_sms = p->num_sms;
   t.topk = p->desc.topk;
   t.topk_ld = a.topk_ld;
   t.sbkv = p->sbkv;

@@ -267,8 +267,7 @@ __device__ __forceinline__ int32_t ld_volatile_s32(const int32_t* a) {
 // much later, so that their address translation is cached by then (a cold
 // miss stalls the stores that hit it for microseconds).
 __device__ __forceinline__ void touch_global(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("{\n .reg .b32 t;\n ld.global.cg.b32 t, [%0];\n}" ::"l"(p));
 }
 
 // Adds with release and acquire semantics at GPU scope: this thread's
@@ -1639,6 +1638,342 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? (kJ <= 8 ? 6 : 4) 
                                 p.logits_fill_bf16 ? p.logits_fill_bf16 + static_cast<int64_t>(r) * S : nullptr, sm);
 }
 
+// ---------------------------------------------------------------------------
+// Top-k of a row by one warp: the selection
+// of select_topk (the value range, a 1024-bin histogram over it, the threshold
+// bin's keys sorted; four 8-bit digit passes where that bin holds more than
+// kRangeBin keys; one ordered compaction), with shuffles in place of block
+// barriers, so that a row's chain of steps stays inside one warp, and few
+// instructions per key (the kernel is issue bound). Each pass reads the row
+// again through L2; lane l takes columns 4 (l + 32 i) + q, q < 4, of chunk i
+// (128 columns) as one float4. Chunks wholly below `end` skip the per-column
+// checks. The results are bit-identical to select_topk's.
+// ---------------------------------------------------------------------------
+__device__ void select_topk_warp(const float* L, int S, int e, int k, const int32_t* sidx, int sbkv, int32_t* out,
+                                 int32_t* colo, uint32_t* hist, uint32_t* list, int* list_n) {
+  const int lane = threadIdx.x & 31;
+  const int sb_shift = 31 - __clz(sbkv);
+  if (e <= k) {  // every valid column is selected, in column order
+    for (int c = lane; c < k; c += 32) {
+      out[c] = c < e ? (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1)) : -1;
+      if (colo) colo[c] = c < e ? c : -1;
+    }
+    return;
+  }
+  const float4* L4 = reinterpret_cast<const float4*>(L);
+  const int nfull = e >> 7;            // chunks whose 128 columns are all below e
+  const int nchunks = (e + 127) >> 7;  // chunks with a column below e
+  auto fetch = [&](int i) { return __ldcg(L4 + lane + 32 * i); };
+  auto fetch_tail = [&](int i) {  // a chunk that crosses e: nothing at or past S is read
+    return 4 * (lane + 32 * i) < S ? fetch(i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  // -- value range
+  float vmin = INFINITY, vmax = -INFINITY;
+#pragma unroll 8
+  for (int i = 0; i < nfull; ++i) {
+    const float4 f = fetch(i);
+    vmin = fminf(vmin, fminf(fminf(f.x, f.y), fminf(f.z, f.w)));
+    vmax = fmaxf(vmax, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+  }
+  for (int i = nfull; i < nchunks; ++i) {
+    const int c = 4 * (lane + 32 * i);
+    const float4 f = fetch_tail(i);
+    const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c + q < e) {
+        vmin = fminf(vmin, v[q]);
+        vmax = fmaxf(vmax, v[q]);
+      }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(kFullMask, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, o));
+  }
+  uint32_t prefix = 0;  // selected high bits so far
+  int need = k;         // keys still to take among those matching the prefix
+  int done_bits = 0;
+  bool ranged = false;
+  uint4* hist4 = reinterpret_cast<uint4*>(hist);
+  if (!(vmax > vmin) || !(vmax - vmin < INFINITY)) {
+    if (vmin == vmax) {  // every valid key equal: the first k
+      prefix = ordered_key(vmin);
+      done_bits = 32;
+      ranged = true;
+    }
+  } else {
+    const float scale = static_cast<float>(kRangeBins) / (vmax - vmin);
+    auto bin_of = [&](float v) { return static_cast<int>(fminf((v - vmin) * scale, kRangeBins - 1.f)); };
+    for (int w = lane; w < kRangeBins / 4; w += 32) hist4[w] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) *list_n = 0;
+    __syncwarp();
+#pragma unroll 4
+    for (int i = 0; i < nfull; ++i) {
+      const float4 f = fetch(i);
+      atomicAdd(&hist[bin_of(f.x)], 1u);
+      atomicAdd(&hist[bin_of(f.y)], 1u);
+      atomicAdd(&hist[bin_of(f.z)], 1u);
+      atomicAdd(&hist[bin_of(f.w)], 1u);
+    }
+    for (int i = nfull; i < nchunks; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      const float4 f = fetch_tail(i);
+      const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < e) atomicAdd(&hist[bin_of(v[q])], 1u);
+    }
+    __syncwarp();
+    // descending scan: lane l owns bins kRangeBins - 32 (l + 1) + b, b < 32, the highest first
+    const int b0 = kRangeBins - 32 * (lane + 1);
+    int local = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint4 v = hist4[b0 / 4 + w];
+      local += static_cast<int>(v.x + v.y + v.z + v.w);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int cum = incl - local, tb = 0, above = 0, tcount = 0;
+    const bool owner = cum < need && need <= incl;
+    if (owner)  // the lane whose run of bins holds the k-th key reads them again
+      for (int b = 31; b >= 0; --b) {
+        const int c = static_cast<int>(hist[b0 + b]);
+        if (c > 0 && cum < need && need <= cum + c) {
+          tb = b0 + b;
+          above = cum;
+          tcount = c;
+        }
+        cum += c;
+      }
+    const int src = __ffs(__ballot_sync(kFullMask, owner)) - 1;
+    tb = __shfl_sync(kFullMask, tb, src);
+    above = __shfl_sync(kFullMask, above, src);
+    tcount = __shfl_sync(kFullMask, tcount, src);
+    if (tcount > 0 && tcount <= kRangeBin) {
+      // the bin's (key, column) pairs, in any order (they are sorted next)
+      auto take = [&](float v, int c) {
+        if (bin_of(v) == tb) {
+          const int at = atomicAdd(list_n, 1);
+          if (at < kRangeBin) {
+            list[2 * at] = ordered_key(v);
+            list[2 * at + 1] = static_cast<uint32_t>(c);
+          }
+        }
+      };
+#pragma unroll 4
+      for (int i = 0; i < nfull; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        const float4 f = fetch(i);
+        take(f.x, c);
+        take(f.y, c + 1);
+        take(f.z, c + 2);
+        take(f.w, c + 3);
+      }
+      for (int i = nfull; i < nchunks; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        const float4 f = fetch_tail(i);
+        const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < e) take(v[q], c + q);
+      }
+      __syncwarp();
+      // bitonic sort of kRangeBin = 64 composites (key, ~column), descending:
+      // lane l holds elements l and l + 32
+      uint64_t y[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        y[h] = i < tcount ? (static_cast<uint64_t>(list[2 * i]) << 32) | (0xFFFFFFFFu - list[2 * i + 1]) : 0ull;
+      }
+#pragma unroll
+      for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            const bool desc = (i & size) == 0;
+            if (stride == 32) {
+              if (h == 0 && (desc ? (y[0] < y[1]) : (y[0] > y[1]))) {
+                const uint64_t t = y[0];
+                y[0] = y[1];
+                y[1] = t;
+              }
+            } else {
+              const uint64_t z = __shfl_xor_sync(kFullMask, y[h], stride);
+              const bool take_max = ((i & stride) == 0) == desc;
+              y[h] = take_max ? (y[h] > z ? y[h] : z) : (y[h] < z ? y[h] : z);
+            }
+          }
+        }
+      }
+      // the (need - above)-th largest is the threshold; how many equal keys are taken
+      const int want = need - above;
+      const int at = want - 1;
+      const uint32_t tkey = static_cast<uint32_t>(__shfl_sync(kFullMask, y[at >> 5], at & 31) >> 32);
+      int eq = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) eq += (lane + 32 * h < want && static_cast<uint32_t>(y[h] >> 32) == tkey) ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) eq += __shfl_xor_sync(kFullMask, eq, o);
+      prefix = tkey;
+      need = eq;
+      done_bits = 32;
+      ranged = true;
+    }
+  }
+  if (!ranged) {
+    // four 8-bit digit passes over a 256-bin histogram; lane l owns bins 255 - 8 l - b
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - done_bits;
+      __syncwarp();
+      for (int w = lane; w < 256 / 4; w += 32) hist4[w] = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      for (int i = 0; i < nchunks; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        const float4 f = fetch_tail(i);
+        const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = ordered_key(v[q]);
+          if (c + q < e && (done_bits == 0 || (key >> (32 - done_bits)) == prefix))
+            atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+      }
+      __syncwarp();
+      const int b0 = 256 - 8 * (lane + 1);
+      int local = 0;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint4 v = hist4[b0 / 4 + w];
+        local += static_cast<int>(v.x + v.y + v.z + v.w);
+      }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int cum = incl - local, sb = 0, above = 0, scount = 0;
+      const bool owner = cum < need && need <= incl;
+      if (owner)
+        for (int b = 7; b >= 0; --b) {
+          const int c = static_cast<int>(hist[b0 + b]);
+          if (c > 0 && cum < need && need <= cum + c) {
+            sb = b0 + b;
+            above = cum;
+            scount = c;
+          }
+          cum += c;
+        }
+      const int src = __ffs(__ballot_sync(kFullMask, owner)) - 1;
+      sb = __shfl_sync(kFullMask, sb, src);
+      above = __shfl_sync(kFullMask, above, src);
+      scount = __shfl_sync(kFullMask, scount, src);
+      prefix = (prefix << 8) | static_cast<uint32_t>(sb);
+      need -= above;
+      done_bits += 8;
+      if (need == scount) break;  // the whole bin is taken
+    }
+  }
+  // selected: keys whose top done_bits bits are above the prefix, and the
+  // first `need` of those equal to it, in column order. A selected column's
+  // slot is the number of selected columns before it; a lane's four columns
+  // are consecutive, so its selected ones take consecutive slots.
+  const uint32_t mask = ~0u << (32 - done_bits);
+  const uint32_t pfx = prefix << (32 - done_bits);
+  int base_g = 0, base_e = 0;
+  auto compact = [&](int i, const float4& f, bool check) {
+    const int c = 4 * (lane + 32 * i);
+    const float v[4] = {f.x, f.y, f.z, f.w};
+    bool g[4], eq[4];
+    uint32_t packed = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t kk = ordered_key(v[q]) & mask;
+      const bool ok = !check || c + q < e;
+      g[q] = ok && kk > pfx;
+      eq[q] = ok && kk == pfx;
+      packed += (g[q] ? 0x10000u : 0u) + (eq[q] ? 1u : 0u);
+    }
+    uint32_t incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t tot = __shfl_sync(kFullMask, incl, 31);
+    const uint32_t pre = incl - packed;
+    int pe = base_e + static_cast<int>(pre & 0xffffu);
+    int slot = base_g + static_cast<int>(pre >> 16) + min(pe, need);
+    base_g += static_cast<int>(tot >> 16);
+    base_e += static_cast<int>(tot & 0xffffu);
+    if (packed == 0) return;
+    const int tok = (sidx[c >> sb_shift] << sb_shift) | (c & (sbkv - 1));  // a lane's columns share a sub-block
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool sel = g[q] || (eq[q] && pe < need);
+      pe += eq[q] ? 1 : 0;
+      if (sel && slot < k) {
+        out[slot] = tok + q;
+        if (colo) colo[slot] = c + q;
+        ++slot;
+      }
+    }
+  };
+#pragma unroll 2
+  for (int i = 0; i < nfull; ++i) compact(i, fetch(i), false);
+  for (int i = nfull; i < nchunks; ++i) compact(i, fetch_tail(i), true);
+}
+
+// One row per warp at a time; one CTA of kTopkWarps warps per SM (at most
+// #SM CTAs), rows dealt round robin: CTA b, warp w takes rows b + G (w + 32 j).
+// Rows, not CTAs, balance the SMs: the kernel is issue bound, and CTAs that
+// start early (on the SMs the previous kernel frees first) would otherwise
+// stack up there. No block barrier. Dynamic shared memory per warp: a
+// 1024-bin histogram, the threshold bin's list and its count, the row's
+// sparse sub-block ids.
+constexpr int kTopkWarps = 32;
+constexpr int kTopkWarpMaxCols = 4096;  // rows this wide or narrower take the warp kernel
+
+__host__ __device__ constexpr int topk_warp_words(int nsb) { return kRangeBins + 2 * kRangeBin + 4 + ((nsb + 3) & ~3); }
+
+__global__ void __launch_bounds__(32 * kTopkWarps, 1) topk_warp_kernel(const __grid_constant__ TopkParams p) {
+  extern __shared__ __align__(16) uint32_t topk_warp_smem_raw[];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.num_cols;
+  uint32_t* hist = topk_warp_smem_raw + static_cast<size_t>(warp) * topk_warp_words(p.nsb);
+  uint32_t* list = hist + kRangeBins;
+  int* list_n = reinterpret_cast<int*>(list + 2 * kRangeBin);
+  int32_t* sidx = reinterpret_cast<int32_t*>(list + 2 * kRangeBin + 4);
+  for (int r = blockIdx.x + gridDim.x * warp; r < p.rows; r += gridDim.x * kTopkWarps) {
+    __syncwarp();  // the previous row's reads of the scratch are done
+    const int32_t* srow = p.sparse_indices + static_cast<int64_t>(r) * p.nsb;
+    for (int i = lane; i < p.nsb; i += 32) sidx[i] = __ldcg(srow + i);
+    int e = __ldcg(p.end + r);
+    e = e < 0 ? 0 : (e > S ? S : e);
+    if (p.logits_fill)
+      for (int c = e + lane; c < S; c += 32) p.logits_fill[static_cast<int64_t>(r) * S + c] = -INFINITY;
+    if (p.logits_fill_bf16)
+      for (int c = e + lane; c < S; c += 32) p.logits_fill_bf16[static_cast<int64_t>(r) * S + c] = kBf16NegInf;
+    __syncwarp();
+    select_topk_warp(p.logits + static_cast<int64_t>(r) * S, S, e, p.topk, sidx, p.sbkv,
+                     p.topk_out + static_cast<int64_t>(r) * p.topk_ld,
+                     p.col_indices ? p.col_indices + static_cast<int64_t>(r) * p.topk : nullptr, hist, list, list_n);
+  }
+}
+
+size_t topk_warp_smem(int nsb) { return static_cast<size_t>(kTopkWarps) * topk_warp_words(nsb) * 4; }
+
 // ===========================================================================
 // Paged -> contiguous K gather: one thread per workspace row.
 // ===========================================================================
@@ -2338,6 +2673,7 @@ cudaError_t prepare_kernels(int n_mma) {
                        reinterpret_cast<const void*>(&topk_kernel<256, 16>),
                        reinterpret_cast<const void*>(&topk_kernel<512, 16>),
                        reinterpret_cast<const void*>(&topk_kernel<512, 32>),
+                       reinterpret_cast<const void*>(&topk_warp_kernel),
                        reinterpret_cast<const void*>(&expand_kernel),
                        reinterpret_cast<const void*>(&gather_kernel),
                        reinterpret_cast<const void*>(&source_layout_kernel),
@@ -2373,6 +2709,10 @@ cudaError_t prepare_kernels(int n_mma) {
 
   err = cudaFuncSetAttribute(source_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSourceMaxBlocks * 8);
+  if (err != cudaSuccess) return err;
+  // the widest rows of the warp top-k: kTopkWarpMaxCols columns in sub-blocks of 16
+  err = cudaFuncSetAttribute(topk_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(topk_warp_smem(kTopkWarpMaxCols / 16)));
   if (err != cudaSuccess) return err;
   return cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kExpandWarps * 2 * 512 * 4);
@@ -2462,6 +2802,11 @@ cudaError_t launch_row_cluster(const ScoreParams& p, const CUtensorMap& tm_q, si
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(p.nsb) * 4;
+  // narrow rows: a warp per row (float4 reads of the logits)
+  if (p.num_cols <= kTopkWarpMaxCols && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0 && p.num_cols % 4 == 0) {
+    const int grid = p.rows < p.num_sms ? p.rows : p.num_sms;
+    return launch_pdl(topk_warp_kernel, static_cast<unsigned>(grid), 32 * kTopkWarps, topk_warp_smem(p.nsb), stream, p);
+  }
   if (p.num_cols <= 8 * 256) return launch_pdl(topk_kernel<256, 8>, p.rows, 256, smem, stream, p);
   if (p.num_cols <= 16 * 256) return launch_pdl(topk_kernel<256, 16>, p.rows, 256, smem, stream, p);
   if (p.num_cols <= 16 * 512) return launch_pdl(topk_kernel<512, 16>, p.rows, 512, smem, stream, p);

@@ -127,6 +127,7 @@ struct ScoreParams {
 
 struct TopkParams {
   int32_t rows;
+  int32_t num_sms;  // CTAs of the warp-per-row kernel: at most one per SM
   int32_t topk;
   int32_t topk_ld;
   int32_t sbkv;
