@@ -1647,7 +1647,8 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? (kJ <= 8 ? 6 : 4) 
 // instructions per key (the kernel is issue bound). Each pass reads the row
 // again through L2; lane l takes columns 4 (l + 32 i) + q, q < 4, of chunk i
 // (128 columns) as one float4. Chunks wholly below `end` skip the per-column
-// checks. The results are bit-identical to select_topk's.
+// checks. The histogram's bins differ from select_topk's (a sampled range),
+// the selection does not: it is exact either way.
 // ---------------------------------------------------------------------------
 __device__ void select_topk_warp(const float* L, int S, int e, int k, const int32_t* sidx, int sbkv, int32_t* out,
                                  int32_t* colo, uint32_t* hist, uint32_t* list, int* list_n) {
@@ -1667,29 +1668,48 @@ __device__ void select_topk_warp(const float* L, int S, int e, int k, const int3
   auto fetch_tail = [&](int i) {  // a chunk that crosses e: nothing at or past S is read
     return 4 * (lane + 32 * i) < S ? fetch(i) : make_float4(0.f, 0.f, 0.f, 0.f);
   };
-  // -- value range
+  // -- value range of the histogram: from a sample (each lane's first four
+  // columns); keys outside it fall into the end bins. Any monotone binning
+  // finds the threshold exactly (its bin's keys are sorted next); a row whose
+  // sample has no spread takes the exact range (one more pass).
   float vmin = INFINITY, vmax = -INFINITY;
-#pragma unroll 8
-  for (int i = 0; i < nfull; ++i) {
-    const float4 f = fetch(i);
-    vmin = fminf(vmin, fminf(fminf(f.x, f.y), fminf(f.z, f.w)));
-    vmax = fmaxf(vmax, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
-  }
-  for (int i = nfull; i < nchunks; ++i) {
-    const int c = 4 * (lane + 32 * i);
-    const float4 f = fetch_tail(i);
+  {
+    const float4 f = fetch_tail(0);
     const float v[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (c + q < e) {
+      if (4 * lane + q < e) {
         vmin = fminf(vmin, v[q]);
         vmax = fmaxf(vmax, v[q]);
       }
   }
+  auto warp_range = [&]() {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    vmin = fminf(vmin, __shfl_xor_sync(kFullMask, vmin, o));
-    vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, o));
+    for (int o = 16; o > 0; o >>= 1) {
+      vmin = fminf(vmin, __shfl_xor_sync(kFullMask, vmin, o));
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, o));
+    }
+  };
+  warp_range();
+  if (!(vmax > vmin) || !(vmax - vmin < INFINITY)) {
+#pragma unroll 8
+    for (int i = 0; i < nfull; ++i) {
+      const float4 f = fetch(i);
+      vmin = fminf(vmin, fminf(fminf(f.x, f.y), fminf(f.z, f.w)));
+      vmax = fmaxf(vmax, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+    }
+    for (int i = nfull; i < nchunks; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      const float4 f = fetch_tail(i);
+      const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < e) {
+          vmin = fminf(vmin, v[q]);
+          vmax = fmaxf(vmax, v[q]);
+        }
+    }
+    warp_range();
   }
   uint32_t prefix = 0;  // selected high bits so far
   int need = k;         // keys still to take among those matching the prefix
@@ -1703,8 +1723,11 @@ __device__ void select_topk_warp(const float* L, int S, int e, int k, const int3
       ranged = true;
     }
   } else {
+    // bin = clamp((v - vmin) scale, 0, kRangeBins - 1): non-decreasing in v
+    // (the conversion saturates below 0; NaN goes to the top bin)
     const float scale = static_cast<float>(kRangeBins) / (vmax - vmin);
-    auto bin_of = [&](float v) { return static_cast<int>(fminf((v - vmin) * scale, kRangeBins - 1.f)); };
+    const float offset = -vmin * scale;
+    auto bin_of = [&](float v) { return static_cast<int>(__float2uint_rz(fminf(fmaf(v, scale, offset), kRangeBins - 1.f))); };
     for (int w = lane; w < kRangeBins / 4; w += 32) hist4[w] = make_uint4(0u, 0u, 0u, 0u);
     if (lane == 0) *list_n = 0;
     __syncwarp();
@@ -1766,7 +1789,7 @@ __device__ void select_topk_warp(const float* L, int S, int e, int k, const int3
           }
         }
       };
-#pragma unroll 4
+#pragma unroll 8
       for (int i = 0; i < nfull; ++i) {
         const int c = 4 * (lane + 32 * i);
         const float4 f = fetch(i);
@@ -1890,14 +1913,14 @@ __device__ void select_topk_warp(const float* L, int S, int e, int k, const int3
   const uint32_t mask = ~0u << (32 - done_bits);
   const uint32_t pfx = prefix << (32 - done_bits);
   int base_g = 0, base_e = 0;
-  auto compact = [&](int i, const float4& f, bool check) {
+  auto compact = [&](int i, const float4& f, bool check, bool masked) {
     const int c = 4 * (lane + 32 * i);
     const float v[4] = {f.x, f.y, f.z, f.w};
     bool g[4], eq[4];
     uint32_t packed = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t kk = ordered_key(v[q]) & mask;
+      const uint32_t kk = masked ? ordered_key(v[q]) & mask : ordered_key(v[q]);
       const bool ok = !check || c + q < e;
       g[q] = ok && kk > pfx;
       eq[q] = ok && kk == pfx;
@@ -1928,9 +1951,14 @@ __device__ void select_topk_warp(const float* L, int S, int e, int k, const int3
       }
     }
   };
+  if (done_bits == 32) {
 #pragma unroll 2
-  for (int i = 0; i < nfull; ++i) compact(i, fetch(i), false);
-  for (int i = nfull; i < nchunks; ++i) compact(i, fetch_tail(i), true);
+    for (int i = 0; i < nfull; ++i) compact(i, fetch(i), false, false);
+  } else {
+#pragma unroll 2
+    for (int i = 0; i < nfull; ++i) compact(i, fetch(i), false, true);
+  }
+  for (int i = nfull; i < nchunks; ++i) compact(i, fetch_tail(i), true, true);
 }
 
 // One row per warp at a time; one CTA of kTopkWarps warps per SM (at most
