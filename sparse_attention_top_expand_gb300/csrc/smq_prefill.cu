@@ -69,12 +69,21 @@ __device__ __forceinline__ void status_or(int32_t* s, int code) { atomicOr(s, co
 __device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ uint16_t round_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// Two independent fp32 fused multiply-adds, each rounded to nearest even.
-__device__ __forceinline__ void fma2(float2& acc, float wa, float wb, float xa, float xb) {
-  asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%0, %1};\n"
-      " fma.rn.f32x2 c, a, b, c;\n mov.b64 {%0, %1}, c;\n}"
-      : "+f"(acc.x), "+f"(acc.y)
-      : "f"(wa), "f"(wb), "f"(xa), "f"(xb));
+// acc += w * (max(x0, 0), max(x1, 0)): two fp32 fused multiply-adds, each
+// rounded to nearest even, on register pairs. The accumulator and the weight
+// pair stay packed (b64) across calls; the two ReLU results are made inside
+// the statement, so they can be allocated as the pair the packed FMA reads.
+__device__ __forceinline__ void relu_fma2(uint64_t& acc, uint64_t w, float x0, float x1) {
+  asm("{\n .reg .f32 a, b;\n .reg .b64 x;\n max.f32 a, %2, 0f00000000;\n max.f32 b, %3, 0f00000000;\n"
+      " mov.b64 x, {a, b};\n fma.rn.f32x2 %0, %1, x, %0;\n}"
+      : "+l"(acc)
+      : "l"(w), "f"(x0), "f"(x1));
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
 }
 
 // Entry j of a row's sparse list: whether it names a sub-block inside the
@@ -601,7 +610,7 @@ __global__ void __launch_bounds__(kBmThreads, 1)
       // Two halves of 32 heads: the second half's loads are this warp's last
       // reads of the accumulator. Heads h = 0, 1 (mod 4) accumulate in lo and
       // h = 2, 3 (mod 4) in hi, each in head order.
-      float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+      uint64_t lo = 0, hi = 0;  // (+0, +0) as packed pairs
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t v[32];
@@ -615,18 +624,19 @@ __global__ void __launch_bounds__(kBmThreads, 1)
           if (lane == 0) mbar_arrive(acc_empty(a));
         }
         if (row < 0) continue;
-        const float4* w4 = reinterpret_cast<const float4*>(prm + 32) + 8 * half;
+        const ulonglong2* w4 = reinterpret_cast<const ulonglong2*>(prm + 32) + 8 * half;
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 w = w4[h4];
+          const ulonglong2 w = w4[h4];  // weights of heads 4 h4 .. 4 h4 + 3 as two pairs
           const uint32_t* x = v + 4 * h4;
-          fma2(lo, w.x, w.y, fmaxf(__uint_as_float(x[0]), 0.f), fmaxf(__uint_as_float(x[1]), 0.f));
-          fma2(hi, w.z, w.w, fmaxf(__uint_as_float(x[2]), 0.f), fmaxf(__uint_as_float(x[3]), 0.f));
+          relu_fma2(lo, w.x, __uint_as_float(x[0]), __uint_as_float(x[1]));
+          relu_fma2(hi, w.y, __uint_as_float(x[2]), __uint_as_float(x[3]));
         }
       }
       if (row >= 0) {
         const float qs = reinterpret_cast<const float*>(prm + 32)[kBmHeads];
-        const float logit = ((lo.x + lo.y) + (hi.x + hi.y)) * qs;
+        const float2 l = unpack2(lo), h = unpack2(hi);
+        const float logit = ((l.x + l.y) + (h.x + h.y)) * qs;
         const uint32_t c0m = static_cast<uint32_t>(gd->c0m[e]);
         const uint32_t mask = c0m >> 24;
         if ((mask >> sl) & 1u) {

@@ -77,21 +77,35 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase is not
+// complete sleeps until it completes (waking within a few hundred cycles of
+// the last arrival) or until about `ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.b32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kWaitSleepNs = 20000;  // the longest sleep of one test
+
 // Wait for the phase with the given parity to complete. Gives up after
-// `limit_ns` or once *abort becomes non-zero; returns false then. The clock and
-// the abort flag are read only every 256 polls.
+// `limit_ns` or once *abort becomes non-zero; returns false then. Each test
+// sleeps until the phase completes (or kWaitSleepNs), so a waiting thread
+// issues a handful of instructions per wait instead of polling; the clock and
+// the abort flag are read after every test that fails.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort) return false;
-      const uint64_t now = global_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > limit_ns) return false;
-    }
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
