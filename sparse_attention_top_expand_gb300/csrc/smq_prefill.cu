@@ -69,13 +69,16 @@ __device__ __forceinline__ void status_or(int32_t* s, int code) { atomicOr(s, co
 __device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ uint16_t round_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// acc += w * (max(x0, 0), max(x1, 0)): two fp32 fused multiply-adds, each
-// rounded to nearest even, on register pairs. The accumulator and the weight
-// pair stay packed (b64) across calls; the two ReLU results are made inside
-// the statement, so they can be allocated as the pair the packed FMA reads.
-__device__ __forceinline__ void relu_fma2(uint64_t& acc, uint64_t w, float x0, float x1) {
-  asm("{\n .reg .f32 a, b;\n .reg .b64 x;\n max.f32 a, %2, 0f00000000;\n max.f32 b, %3, 0f00000000;\n"
-      " mov.b64 x, {a, b};\n fma.rn.f32x2 %0, %1, x, %0;\n}"
+// acc += w * (x0 + |x0|, x1 + |x1|) = 2 w ReLU(x): two fp32 fused
+// multiply-adds, each rounded to nearest even, on register pairs. x + |x| is
+// exactly 2 max(x, 0) and runs on the FMA pipe (a max would take the ALU
+// pipe, which the epilogue's integer work already loads); the caller halves
+// the sum, exactly. The accumulator and the weight pair stay packed (b64)
+// across calls; the two sums are made inside the statement, so they can be
+// allocated as the pair the packed FMA reads.
+__device__ __forceinline__ void relu2_fma2(uint64_t& acc, uint64_t w, float x0, float x1) {
+  asm("{\n .reg .f32 a, b, c, d;\n .reg .b64 x;\n abs.f32 c, %2;\n abs.f32 d, %3;\n add.f32 a, %2, c;\n"
+      " add.f32 b, %3, d;\n mov.b64 x, {a, b};\n fma.rn.f32x2 %0, %1, x, %0;\n}"
       : "+l"(acc)
       : "l"(w), "f"(x0), "f"(x1));
 }
@@ -629,14 +632,14 @@ __global__ void __launch_bounds__(kBmThreads, 1)
         for (int h4 = 0; h4 < 8; ++h4) {
           const ulonglong2 w = w4[h4];  // weights of heads 4 h4 .. 4 h4 + 3 as two pairs
           const uint32_t* x = v + 4 * h4;
-          relu_fma2(lo, w.x, __uint_as_float(x[0]), __uint_as_float(x[1]));
-          relu_fma2(hi, w.y, __uint_as_float(x[2]), __uint_as_float(x[3]));
+          relu2_fma2(lo, w.x, __uint_as_float(x[0]), __uint_as_float(x[1]));
+          relu2_fma2(hi, w.y, __uint_as_float(x[2]), __uint_as_float(x[3]));
         }
       }
       if (row >= 0) {
         const float qs = reinterpret_cast<const float*>(prm + 32)[kBmHeads];
-        const float2 l = unpack2(lo), h = unpack2(hi);
-        const float logit = ((l.x + l.y) + (h.x + h.y)) * qs;
+        const float2 l = unpack2(lo), h = unpack2(hi);  // twice the head sums, exactly
+        const float logit = ((l.x + l.y) + (h.x + h.y)) * (0.5f * qs);
         const uint32_t c0m = static_cast<uint32_t>(gd->c0m[e]);
         const uint32_t mask = c0m >> 24;
         if ((mask >> sl) & 1u) {
