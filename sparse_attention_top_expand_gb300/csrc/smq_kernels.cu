@@ -1244,7 +1244,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     bool need_end = false;
     uint32_t quse = 0;
     float qs = 0.f;
-    float w[kN];
+    // head weights: packed pairs (2j, 2j + 1) for the packed FMA at 64 heads;
+    // scalars at 128 heads (pairs would not fit the registers)
+    constexpr bool kPacked = kN == 64;
+    uint64_t w2[kPacked ? kN / 2 : 1];
+    float w[kPacked ? 1 : kN];
     bool ok = true;
     for (int ie = 0; ie < n && ok; ++ie) {
       const int64_t t = t_begin + ie;
@@ -1260,8 +1264,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if constexpr (!kFused) e = meta[qb].end;
         qs = meta[qb].q_scale;
         const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w + qb * lay.w_stride);
+        if constexpr (kPacked) {
 #pragma unroll
-        for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+          for (int j = 0; j < kN / 2; ++j)
+            w2[j] = pack2(2 * j < H ? bf16_to_f32(wsm[2 * j]) : 0.f, 2 * j + 1 < H ? bf16_to_f32(wsm[2 * j + 1]) : 0.f);
+        } else {
+#pragma unroll
+          for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+        }
       }
       const bool last_of_row = (t + 1 >= t_end) || (t + 1 >= prefix[r + 1]);
       const int a = ie % NA;
@@ -1276,8 +1286,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
-        // four independent partial sums keep the FMA pipe busy instead of one
-        // 64-deep dependent chain
+        // four independent partial sums (heads h mod 4; two packed pairs at 64
+        // heads) keep the FMA pipe busy instead of one 64-deep dependent chain
+        uint64_t lo = 0, hi = 0;
         float acc4[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t tacc = tmem + (a * kHalves + h) * kN + lane_base;
 #pragma unroll
@@ -1291,18 +1302,35 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acc_empty(a));
           }
+          if constexpr (kPacked) {
 #pragma unroll
-          for (int hh = 0; hh < 16; ++hh)
-            acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+            for (int hh = 0; hh < 16; hh += 4) {
+              relu2_fma2(lo, w2[(c + hh) / 2], __uint_as_float(v0[hh]), __uint_as_float(v0[hh + 1]));
+              relu2_fma2(hi, w2[(c + hh) / 2 + 1], __uint_as_float(v0[hh + 2]), __uint_as_float(v0[hh + 3]));
+            }
 #pragma unroll
-          for (int hh = 0; hh < 16; ++hh)
-            acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
+            for (int hh = 0; hh < 16; hh += 4) {
+              relu2_fma2(lo, w2[(c + 16 + hh) / 2], __uint_as_float(v1[hh]), __uint_as_float(v1[hh + 1]));
+              relu2_fma2(hi, w2[(c + 16 + hh) / 2 + 1], __uint_as_float(v1[hh + 2]), __uint_as_float(v1[hh + 3]));
+            }
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < 16; ++hh)
+              acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+#pragma unroll
+            for (int hh = 0; hh < 16; ++hh)
+              acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
+          }
         }
-        const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        // the head sums (twice them, exactly, from the packed form)
+        const float2 l2 = kPacked ? unpack2(lo) : make_float2(acc4[0], acc4[1]);
+        const float2 h2 = kPacked ? unpack2(hi) : make_float2(acc4[2], acc4[3]);
+        const float qscale = kPacked ? 0.5f * qs : qs;
+        const float logit = ((l2.x + l2.y) + (h2.x + h2.y)) * qscale;
         const int col = static_cast<int>(t - prefix[r]) * kTileM + h * kMmaM + m;
         if (col < e) {
-          p.logits[static_cast<int64_t>(row) * S + col] = acc * qs;
-          if (p.logits_bf16) p.logits_bf16[static_cast<int64_t>(row) * S + col] = to_bf16(acc * qs);
+          p.logits[static_cast<int64_t>(row) * S + col] = logit;
+          if (p.logits_bf16) p.logits_bf16[static_cast<int64_t>(row) * S + col] = to_bf16(logit);
         }
       }
       if (warp == 2 && lane == 0 && ie == 0) SMQ_MARK(11);
@@ -2385,10 +2413,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int m = 32 * q4 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = n > 0 ? warp_wait(bar_q_full, 0, abort_flag, static_cast<uint64_t>(p.wait_ns)) : true;
-    float w[kN];
+    // head weights: packed pairs (2j, 2j + 1) for the packed FMA at 64 heads;
+    // scalars at 128 heads (pairs would not fit the registers)
+    constexpr bool kPacked = kN == 64;
+    uint64_t w2[kPacked ? kN / 2 : 1];
+    float w[kPacked ? 1 : kN];
     const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + lay.w);
+    if constexpr (kPacked) {
 #pragma unroll
-    for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+      for (int j = 0; j < kN / 2; ++j)
+        w2[j] = pack2(2 * j < H ? bf16_to_f32(wsm[2 * j]) : 0.f, 2 * j + 1 < H ? bf16_to_f32(wsm[2 * j + 1]) : 0.f);
+    } else {
+#pragma unroll
+      for (int h = 0; h < kN; ++h) w[h] = h < H ? bf16_to_f32(wsm[h]) : 0.f;
+    }
     const float qs = n > 0 ? *qscale_sm : 0.f;
     float* lout = p.logits_out ? p.logits_out + static_cast<int64_t>(r) * S : nullptr;
     uint16_t* lout16 = p.logits_bf16 ? p.logits_bf16 + static_cast<int64_t>(r) * S : nullptr;
@@ -2402,7 +2440,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t lo = 0, hi = 0;  // heads h mod 4: two packed pairs of partial sums (64 heads)
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};  // or four scalars (128 heads)
         const uint32_t tacc = tmem + (a * kHalves + h) * kN + lane_base;
 #pragma unroll
         for (int c = 0; c < kN; c += 32) {
@@ -2415,14 +2454,31 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acc_empty(a));
           }
+          if constexpr (kPacked) {
 #pragma unroll
-          for (int hh = 0; hh < 16; ++hh)
-            acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+            for (int hh = 0; hh < 16; hh += 4) {
+              relu2_fma2(lo, w2[(c + hh) / 2], __uint_as_float(v0[hh]), __uint_as_float(v0[hh + 1]));
+              relu2_fma2(hi, w2[(c + hh) / 2 + 1], __uint_as_float(v0[hh + 2]), __uint_as_float(v0[hh + 3]));
+            }
 #pragma unroll
-          for (int hh = 0; hh < 16; ++hh)
-            acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
+            for (int hh = 0; hh < 16; hh += 4) {
+              relu2_fma2(lo, w2[(c + 16 + hh) / 2], __uint_as_float(v1[hh]), __uint_as_float(v1[hh + 1]));
+              relu2_fma2(hi, w2[(c + 16 + hh) / 2 + 1], __uint_as_float(v1[hh + 2]), __uint_as_float(v1[hh + 3]));
+            }
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < 16; ++hh)
+              acc4[hh & 3] = fmaf(w[c + hh], fmaxf(__uint_as_float(v0[hh]), 0.f), acc4[hh & 3]);
+#pragma unroll
+            for (int hh = 0; hh < 16; ++hh)
+              acc4[hh & 3] = fmaf(w[c + 16 + hh], fmaxf(__uint_as_float(v1[hh]), 0.f), acc4[hh & 3]);
+          }
         }
-        const float logit = ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3])) * qs;
+        // the head sums (twice them, exactly, from the packed form)
+        const float2 l2 = kPacked ? unpack2(lo) : make_float2(acc4[0], acc4[1]);
+        const float2 h2 = kPacked ? unpack2(hi) : make_float2(acc4[2], acc4[3]);
+        const float qscale = kPacked ? 0.5f * qs : qs;
+        const float logit = ((l2.x + l2.y) + (h2.x + h2.y)) * qscale;
         const int lc = ie * kTileM + h * kMmaM + m;  // local column
         const int col = c0 + lc;
         if (col < e) lg[col] = logit;

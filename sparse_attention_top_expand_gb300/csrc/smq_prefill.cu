@@ -69,26 +69,6 @@ __device__ __forceinline__ void status_or(int32_t* s, int code) { atomicOr(s, co
 __device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ uint16_t round_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// acc += w * (x0 + |x0|, x1 + |x1|) = 2 w ReLU(x): two fp32 fused
-// multiply-adds, each rounded to nearest even, on register pairs. x + |x| is
-// exactly 2 max(x, 0) and runs on the FMA pipe (a max would take the ALU
-// pipe, which the epilogue's integer work already loads); the caller halves
-// the sum, exactly. The accumulator and the weight pair stay packed (b64)
-// across calls; the two sums are made inside the statement, so they can be
-// allocated as the pair the packed FMA reads.
-__device__ __forceinline__ void relu2_fma2(uint64_t& acc, uint64_t w, float x0, float x1) {
-  asm("{\n .reg .f32 a, b, c, d;\n .reg .b64 x;\n abs.f32 c, %2;\n abs.f32 d, %3;\n add.f32 a, %2, c;\n"
-      " add.f32 b, %3, d;\n mov.b64 x, {a, b};\n fma.rn.f32x2 %0, %1, x, %0;\n}"
-      : "+l"(acc)
-      : "l"(w), "f"(x0), "f"(x1));
-}
-
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-
 // Entry j of a row's sparse list: whether it names a sub-block inside the
 // workspace, its window u (relative to the row's ks) and its slot there.
 struct Entry {

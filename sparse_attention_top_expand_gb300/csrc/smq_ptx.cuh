@@ -234,6 +234,33 @@ __device__ __forceinline__ void prefetch_tma_2d(const CUtensorMap* map, int32_t 
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
 }
 
+// ------------------------------------------------------------ packed fp32
+
+// acc += w * (x0 + |x0|, x1 + |x1|) = 2 w ReLU(x): two fp32 fused
+// multiply-adds, each rounded to nearest even, on register pairs (f32x2).
+// x + |x| is exactly 2 max(x, 0) and runs on the FMA pipe, not the ALU pipe a
+// max takes; callers halve the final sum, exactly. The accumulator and the
+// weight pair stay packed (b64) across calls; the two sums are made inside the
+// statement, so they can be allocated as the pair the packed FMA reads.
+__device__ __forceinline__ void relu2_fma2(uint64_t& acc, uint64_t w, float x0, float x1) {
+  asm("{\n .reg .f32 a, b, c, d;\n .reg .b64 x;\n abs.f32 c, %2;\n abs.f32 d, %3;\n add.f32 a, %2, c;\n"
+      " add.f32 b, %3, d;\n mov.b64 x, {a, b};\n fma.rn.f32x2 %0, %1, x, %0;\n}"
+      : "+l"(acc)
+      : "l"(w), "f"(x0), "f"(x1));
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
