@@ -150,6 +150,9 @@ size_t score_smem_bytes(int n_mma, int heads, int rows) {
   return ScoreLayout(n_mma, heads, rows).total + 1024;
 }
 
+__device__ int expand_row_in_warp(int ncb, int64_t cbs, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
+                                   int lane);
+
 // ===========================================================================
 // Candidate expansion: one warp per row.
 // ===========================================================================
@@ -165,6 +168,25 @@ __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_
   const int64_t ks = p.row_ks ? p.row_ks[r] : 0;
   int64_t L = static_cast<int64_t>(p.row_ke[r]) - ks;
   if (L < 0) L = 0;
+  const int spb = p.cbs / p.sbkv;
+  int32_t* si = p.sparse_indices + static_cast<int64_t>(r) * p.nsb;
+  if (p.ncb <= kMaxFusedBlocks) {  // one or two ids per lane: the warp's sorting network
+    const int32_t* cbr = p.candidate_blocks + static_cast<int64_t>(r) * p.ncb;
+    const int c0 = lane < p.ncb ? cbr[lane] : -1, c1 = lane + 32 < p.ncb ? cbr[lane + 32] : -1;
+    int nkept = 0;
+    const int cols = expand_row_in_warp(p.ncb, p.cbs, L, c0, c1, cand, &nkept, lane);
+    for (int slot = lane; slot < p.nsb; slot += 32) {
+      const int k = slot / spb;
+      int v = -1;
+      if (k < nkept) {
+        const int sub = cand[k] * spb + slot % spb;
+        if (static_cast<int64_t>(sub) * p.sbkv < L) v = sub;
+      }
+      si[slot] = v;
+    }
+    if (lane == 0) p.end[r] = cols;
+    return;
+  }
   for (int i = lane; i < p.ncb; i += 32) cand[i] = p.candidate_blocks[static_cast<int64_t>(r) * p.ncb + i];
   __syncwarp();
   // keep a block if it is in range and its first occurrence; others -> INT_MAX
@@ -177,8 +199,6 @@ __global__ void __launch_bounds__(kExpandWarps * 32) expand_kernel(const __grid_
     kept[i] = keep ? b : INT_MAX;
   }
   __syncwarp();
-  const int spb = p.cbs / p.sbkv;
-  int32_t* si = p.sparse_indices + static_cast<int64_t>(r) * p.nsb;
   int64_t cols = 0;
   int nkept = 0;
   for (int i = lane; i < p.ncb; i += 32) {
@@ -283,13 +303,13 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 // (the same result as expand_kernel): a block is kept if it lies in [0, L)
 // and no earlier candidate has the same id; the kept blocks are sorted into
 // sorted[0 .. *nkept_out). Returns the row's column count.
-__device__ int expand_row_in_warp(const ScoreParams& p, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
+__device__ int expand_row_in_warp(int ncb, int64_t cbs, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
                                    int lane);
 
 __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_t* sorted, int* nkept_out, int lane) {
   const int32_t* cb = p.candidate_blocks + static_cast<int64_t>(r) * p.ncb;
-  return expand_row_in_warp(p, L, lane < p.ncb ? cb[lane] : -1, lane + 32 < p.ncb ? cb[lane + 32] : -1, sorted,
-                            nkept_out, lane);
+  return expand_row_in_warp(p.ncb, p.cbs, L, lane < p.ncb ? cb[lane] : -1, lane + 32 < p.ncb ? cb[lane + 32] : -1,
+                            sorted, nkept_out, lane);
 }
 
 // The same with the row's candidates already loaded: lane l holds ids l (c0)
@@ -299,10 +319,8 @@ __device__ int expand_row_in_warp(const ScoreParams& p, int r, int64_t L, int32_
 // sort last as INT_MAX). A sorted id equal to its predecessor is a repeat and is
 // dropped; the rest land in `sorted` at their rank, counted by ballots. Block b
 // holds min(cbs, L - b cbs) columns below L.
-__device__ int expand_row_in_warp(const ScoreParams& p, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
+__device__ int expand_row_in_warp(int ncb, int64_t cbs, int64_t L, int c0, int c1, int32_t* sorted, int* nkept_out,
                                    int lane) {
-  const int ncb = p.ncb;
-  const int64_t cbs = p.cbs;
   auto key = [&](int b, bool live) { return live && b >= 0 && static_cast<int64_t>(b) * cbs < L ? b : INT_MAX; };
   auto block_cols = [&](int b, bool keep) {
     const int64_t rest = keep ? L - static_cast<int64_t>(b) * cbs : 0;
@@ -2049,8 +2067,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     set_status(p.status, kStatusBounds);
     return;
   }
-  const int64_t pos = wrow - start;
-  const int64_t slot = pos / p.page_size;
+  const int pos = static_cast<int>(wrow - start);  // a position within one sequence (int32 lengths)
+  const int slot = pos / p.page_size;
   if (slot >= p.bt_stride) {
     set_status(p.status, kStatusBounds);
     return;
@@ -2060,14 +2078,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     set_status(p.status, kStatusBounds);
     return;
   }
-  const int64_t tok = pos % p.page_size;
+  const int tok = pos - slot * p.page_size;
   const uint8_t* base = p.k_cache + static_cast<int64_t>(page) * p.page_bytes;
   const uint4* src = reinterpret_cast<const uint4*>(base + tok * (kHeadDim / 2));
   uint4* dst = reinterpret_cast<uint4*>(p.k_values + wrow * (kHeadDim / 2));
 #pragma unroll
   for (int i = 0; i < kHeadDim / 32; ++i) dst[i] = src[i];
-  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(base + static_cast<int64_t>(p.page_size) * (kHeadDim / 2) +
-                                                           tok * kScaleWordBytes);
+  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(base + p.page_size * (kHeadDim / 2) + tok * kScaleWordBytes);
   reinterpret_cast<uint32_t*>(p.k_scales)[wrow] = *ssrc;
 }
 
@@ -2268,7 +2285,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     int e = 0;
     if (p.fused) {
       int nkept = 0;
-      const int cols = expand_row_in_warp(p, L, s_c0, s_c1, sorted, &nkept, lane);
+      const int cols = expand_row_in_warp(p.ncb, p.cbs, L, s_c0, s_c1, sorted, &nkept, lane);
       if (lane == 0) SMQ_MARK(18);
       e = cols < 0 ? 0 : (cols > S ? S : cols);
       for (int slot = lane; slot < p.nsb; slot += 32) {
