@@ -310,6 +310,23 @@ def test_prefill_topk_kernel_with_ties(mode):
     check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="sparse", contig=(kv, ks)))
 
 
+def test_prefill_topk_sampled_range_cases():
+    """The warp top-k bins each row over the value range of its first 128
+    columns. Every other page of the cache holds equal keys, so across the
+    rows: a first candidate block of equal keys (the sample has no spread and
+    the exact range is taken), many equal keys outside the sampled range (the
+    threshold bin overflows and the digit passes decide), ties by column."""
+    inp = synth.prefill_chunk(seed=43, seq_lens=(1500, 2300), queries_per_seq=30, num_heads=64, page_size=64,
+                              cbs=128, ncb=8, topk=300)
+    half = inp.geom.page_size * 64
+    inp.k_cache[0::2, :half] = 0x22  # every element 1.0 on even pages
+    inp.k_cache[0::2, half:] = 127
+    plan, dev, status = run_prefill(inp)
+    _ok(status)
+    kv, ks = oracle.gather_reference(inp)
+    check_rows(inp, dev, plan, oracle.reference_rows(inp, mode="sparse", contig=(kv, ks)))
+
+
 def test_zero_rows_is_a_no_op():
     inp = synth.tiny_decode(0)
     plan = tensors.plan_for(inp.geom, max_rows=4)
