@@ -1475,6 +1475,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                             ds.values != nullptr && stk[h] < ds.positions);
         }
       };
+      // Two register slots: each slot's tile is stored, then the slot takes
+      // its next tile at once, so that the next load is out before the other
+      // slot's stores.
       for (int i0 = 0; i0 < n + 2; i0 += 2) {
         const int j0 = i0 - 2;  // the pair whose data sits in the slots
         if (j0 >= 0 && j0 < n) {
@@ -1483,29 +1486,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ok = warp_wait(bar_empty(jl % NS), ((jl / NS) & 1) ^ 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
           if (!ok) break;
           store_tile(v[0], sw[0], j0);
-          if (j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
         }
         if (i0 < n) {
-          // when the pair's second tile is already published (the ring runs ahead),
-          // nothing is waited for; otherwise each tile is waited for, so that the
-          // first loads leave as soon as their tile is published
-          const int il = i0 + 1 < n ? i0 + 1 : i0;
-          bool both = false;
-          if (lane == 0) both = mbar_test_wait(bar_desc_full(il % kDescRing), (il / kDescRing) & 1);
-          both = __shfl_sync(kFullMask, both ? 1 : 0, 0) != 0;
-          __syncwarp();  // orders the other lanes after lane 0's acquire
-          if (!both) {
-            ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
-            if (!ok) break;
-          }
+          ok = warp_wait(bar_desc_full(i0 % kDescRing), (i0 / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
+          if (!ok) break;
           load_tile(v[0], sw[0], i0);
-          if (i0 + 1 < n) {
-            if (!both) {
-              ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag, static_cast<uint64_t>(p.wait_ns));
-              if (!ok) break;
-            }
-            load_tile(v[1], sw[1], i0 + 1);
-          }
+        }
+        if (j0 >= 0 && j0 + 1 < n) store_tile(v[1], sw[1], j0 + 1);
+        if (i0 + 1 < n) {
+          ok = warp_wait(bar_desc_full((i0 + 1) % kDescRing), ((i0 + 1) / kDescRing) & 1, abort_flag,
+                         static_cast<uint64_t>(p.wait_ns));
+          if (!ok) break;
+          load_tile(v[1], sw[1], i0 + 1);
+        }
+        if (i0 < n) {
           __syncwarp();  // every lane has read the entries before they are handed back
           if (lane == 0) {
             mbar_arrive(bar_desc_empty(i0 % kDescRing));
