@@ -2276,34 +2276,44 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #ifdef SMQ_TRACE
     if (__shfl_sync(kFullMask, s_c0 ^ s_c1 ^ s_ke ^ s_brow, 0) != 0x5a5a5a5a && lane == 0) SMQ_MARK(17);
 #endif
-    int e = 0;
+    // Sub-blocks per candidate block and per cache page: shifts where they are
+    // powers of two (the usual case), divisions otherwise.
+    const int spp = p.page_size / sbkv;
+    const int spb_sh = (spb & (spb - 1)) == 0 ? __ffs(spb) - 1 : -1;
+    const int spp_sh = (spp & (spp - 1)) == 0 ? __ffs(spp) - 1 : -1;
+    auto div_spb = [&](int x) { return spb_sh >= 0 ? x >> spb_sh : x / spb; };
+    auto div_spp = [&](int x) { return spp_sh >= 0 ? x >> spp_sh : x / spp; };
+    int e = 0, nkept = 0;
     if (p.fused) {
-      int nkept = 0;
       const int cols = expand_row_in_warp(p.ncb, p.cbs, L, s_c0, s_c1, sorted, &nkept, lane);
       if (lane == 0) SMQ_MARK(18);
       e = cols < 0 ? 0 : (cols > S ? S : cols);
-      for (int slot = lane; slot < p.nsb; slot += 32) {
-        const int k = slot / spb;
-        int v = -1;
-        if (k < nkept) {
-          const int sub = sorted[k] * spb + slot % spb;
-          if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
-        }
-        sidx[slot] = v;
-      }
     } else {
       e = p.end[r];
       e = e < 0 ? 0 : (e > S ? S : e);
       for (int slot = lane; slot < p.nsb; slot += 32) sidx[slot] = p.sparse_indices[static_cast<int64_t>(r) * p.nsb + slot];
     }
+    // the row's sparse sub-block list from the sorted blocks (fused): after
+    // the first block-table loads, off the path to the first tile
+    auto fill_sidx = [&]() {
+      for (int slot = lane; slot < p.nsb; slot += 32) {
+        const int k = div_spb(slot);
+        int v = -1;
+        if (k < nkept) {
+          const int sub = sorted[k] * spb + (slot - k * spb);
+          if (static_cast<int64_t>(sub) * sbkv < L) v = sub;
+        }
+        sidx[slot] = v;
+      }
+    };
     if (lane == 0) st_volatile_s32(end_sm, e);
     if (lane == 0) SMQ_MARK(4);
-    __syncwarp();  // sidx is read by every lane below
-    bool owner = p.fused && rank == 0;  // writes the row's expansion once its first block-table loads are out
+    __syncwarp();  // sidx (passed-in expansion) or sorted (fused) is read by every lane below
+    bool sidx_ready = !p.fused;
+    bool owner = p.fused && rank == 0;  // writes the row's expansion once its first tiles are published
     bool ok = true;
     int it = 0;
     const int tiles_per_batch = 32 / spt;
-    const int spp = p.page_size / sbkv;  // sub-blocks per cache page
     for (int tb = 0; tb < n && ok; tb += tiles_per_batch) {
       const int tl = tb + lane / spt;  // local tile
       const int sub = lane % spt;
@@ -2311,17 +2321,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const bool want = tl < n && col_sub * sbkv < e;
       int pg = -1, tok = 0;
       if (want) {
-        const int sb = sidx[col_sub];
-        const int slot = sb / spp;
+        // columns below end lie in the leading sub-blocks of the kept blocks, all valid
+        int sb;
+        if (p.fused) {
+          const int k = div_spb(col_sub);
+          sb = sorted[k] * spb + (col_sub - k * spb);
+        } else {
+          sb = sidx[col_sub];
+        }
+        const int slot = div_spp(sb);
         tok = (sb - slot * spp) * sbkv;
         if (sb >= 0 && brow >= 0 && brow < p.bt_rows && slot < p.bt_stride)
           pg = p.block_table[static_cast<int64_t>(brow) * p.bt_stride + slot];
-      }
-      if (owner) {
-        for (int slot = lane; slot < p.nsb; slot += 32)
-          p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = sidx[slot];
-        if (lane == 0) p.end_out[r] = e;
-        owner = false;
       }
       int ntok = 0, trow = 0, tpage = 0;
       const uint8_t* vsrc = nullptr;
@@ -2354,6 +2365,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (lane == 0 && it == n - 1) SMQ_MARK(6);
         ++it;
       }
+      if (!sidx_ready) {
+        fill_sidx();
+        sidx_ready = true;
+        __syncwarp();
+      }
+      if (owner) {
+        for (int slot = lane; slot < p.nsb; slot += 32)
+          p.sparse_indices_out[static_cast<int64_t>(r) * p.nsb + slot] = sidx[slot];
+        if (lane == 0) p.end_out[r] = e;
+        owner = false;
+      }
+    }
+    if (!sidx_ready) {  // a CTA without a tile (or one that gave up) still holds the row's list for the top-k
+      fill_sidx();
+      __syncwarp();
     }
     if (owner) {  // a row with no tile in this CTA
       for (int slot = lane; slot < p.nsb; slot += 32)
