@@ -109,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
-// The same wait for a whole warp: lane 0 polls, the warp then resumes together
+// The same wait for a whole warp: lane 0 waits, the warp then resumes together
 // (__syncwarp orders the other lanes after lane 0's acquire).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
